@@ -1,0 +1,406 @@
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--mode sample|greedy] [--impl ours|reference]
+
+One step = one specdec_verify call: the LM head scores all gamma+1
+positions of every sequence in one weight read, then the acceptance scan and
+the residual / bonus draw run. Inputs are synthetic, seeded and resident in
+HBM before the timed region; W_lm (1.05 GB for the default Llama-3-8B head)
+is larger than L2, so no flush is needed between steps. Under torchrun each
+rank runs an independent replica on its own GPU (weak scaling, no
+collective on the data path); the step time is the maximum over ranks.
+
+Prints one JSON line: steps/s (whole job), committed tokens/s, the LM-head
+kernel's roofline fraction (CUDA events inside the timed steps), the fp64
+oracle on the host cores as cpu_baseline, an end-to-end figure through the
+host-pointer entry point, and the SM clocks sampled during the timed region.
+--impl reference times the fp64 oracle itself on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import datetime as _dt
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from target_model_verify_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verify steps/s and committed tokens/s at 1 GB300; % of HBM/tensor roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+LMHEAD_SOURCES = ["target_model_verify_gb300/csrc/lmhead_tc.cu",
+                  "target_model_verify_gb300/csrc/common.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+CPU_BASELINE_SECONDS = 10.0
+REFERENCE_BUDGET_SECONDS = 150.0
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description="verify-step benchmark")
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", default="llama3_8b_head", choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--mode", default="sample", choices=["sample", "greedy"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    return args
+
+
+# --------------------------------------------------------------- helpers --
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f), "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def lmhead_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in LMHEAD_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, mode: str):
+    """DRAM bytes per LM-head launch from a committed ncu summary, if the
+    kernel sources still match the ones it was captured from."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    with open(TRAFFIC_FILE) as f:
+        rec = json.load(f)
+    ent = rec.get(f"{workload}/{mode}")
+    if not ent or ent.get("source_hash") != lmhead_source_hash():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons (100 ms)."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.lines = []
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100", "-i", str(gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [ln for ln in out.splitlines() if ln.strip()]
+
+    def summary(self, t0: float, t1: float):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                ts = _dt.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in inside for k in range(4) if r[3][k] == "Active"})
+        return {"sm_mhz": statistics.median(r[1] for r in inside),
+                "sm_max_mhz": max(r[2] for r in inside), "reasons": reasons,
+                "samples": len(inside)}
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_inputs(inp: dict, mode: int):
+    h = inp["hidden"].float().cpu().double().numpy()
+    W = inp["W_lm"].float().cpu().double().numpy()
+    x = inp["draft_tokens"].cpu().numpy().astype(np.int64)
+    dl = inp["draft_logits"].float().cpu().double().numpy() if mode == wl.SAMPLE else None
+    return h, W, x, dl
+
+
+def time_oracle(w, inp, mode, budget_s: float, min_steps: int = 1):
+    """Full oracle steps on the host cores until the budget is used."""
+    from oracle import verify as ov
+    h, W, x, dl = oracle_inputs(inp, mode)
+    n = 0
+    t0 = time.perf_counter()
+    while n < min_steps or time.perf_counter() - t0 < budget_s:
+        ov.verify(h, W, x, dl, w.temperature, 1000 + n, mode)
+        n += 1
+    return n / (time.perf_counter() - t0), n
+
+
+# ------------------------------------------------------------ our arm --
+
+def run_ours(args, world, rank, local):
+    import target_model_verify_gb300 as tv
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    w = wl.get(args.workload)
+    mode = wl.SAMPLE if args.mode == "sample" else wl.GREEDY
+    inp = wl.generate(w, args.seed + rank, device=device)
+    dl = inp["draft_logits"] if mode == wl.SAMPLE else None
+    ws = tv.alloc_workspace(w.B, w.gamma, w.d, w.V, inp["hidden"].dtype, mode, device=device)
+    K, Wm = args.steps, args.warmup
+    outs = torch.empty(K + Wm, w.B, w.gamma + 1, dtype=torch.int32, device=device)
+    naccs = torch.empty(K + Wm, w.B, dtype=torch.int32, device=device)
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    for e in ev0 + ev1:
+        e.record()          # creates the underlying CUDA event
+    torch.cuda.synchronize()
+
+    def step(i, events=None):
+        tv.verify(inp["hidden"], inp["W_lm"], inp["draft_tokens"], dl, w.temperature,
+                  args.seed * 1_000_003 + i, mode, out_tokens=outs[i], n_accepted=naccs[i],
+                  workspace=ws, events=events)
+
+    sampler = ClockSampler(device.index) if rank == 0 else None
+    time.sleep(0.6 if sampler else 0)
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    start.record()
+    for k in range(K):
+        step(Wm + k, (ev0[k], ev1[k]))
+    end.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed_ms = start.elapsed_time(end)
+    lm_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
+    if sampler:
+        time.sleep(0.2)
+        sampler.stop()
+    st = tv.read_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {tv.status_string(st)}")
+
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    max_ms = float(t.item())
+    nacc = naccs[Wm:].double()
+    tokens_per_step = float((nacc + 1).sum(dim=1).mean().item())
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(tv, w, inp, mode, K, Wm, args, device)
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peaks, peak_kind = load_peaks()
+    steps_per_s = world * K / (max_ms / 1e3)
+    lm_avg_s = float(np.mean(lm_ms)) / 1e3
+    step_s = max_ms / 1e3 / K
+    bytes_alg = w.algorithmic_bytes(mode)
+    lm_bytes = bytes_alg - w.B * w.gamma * 4          # the LM-head kernel does not read x
+    t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9)
+    t_tc = w.flops() / (peaks["bf16_tflops"] * 1e12)
+    tensor_bound = t_tc > t_hbm
+    if tensor_bound:
+        achieved = w.flops() / lm_avg_s / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s"}
+    else:
+        achieved = lm_bytes / lm_avg_s / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = recorded_traffic(args.workload, args.mode)
+    roof["kernel"] = "lmhead_tc_kernel"
+    roof["kernel_us"] = lm_avg_s * 1e6
+    roof["peak_source"] = f"{peak_kind} (MEASURED_PEAKS.json)" if peak_kind == "measured" \
+        else "fallback"
+    roof["algorithmic_bytes"] = lm_bytes
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        v, n = time_oracle(w, inp, mode, CPU_BASELINE_SECONDS)
+        cpu = {"value": v, "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{n} full {args.workload} steps (fp64 NumPy oracle, W converted "
+                         f"to fp64 once outside the timing)"}
+
+    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    line = {
+        "metric": METRIC,
+        "value": steps_per_s,
+        "unit": "steps/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": Wm,
+        "ms_per_step": max_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32",
+        "data": "synthetic (seeded; random-init LM head)",
+        "config": {"workload": args.workload, "B": w.B, "gamma": w.gamma, "d": w.d, "V": w.V,
+                   "mode": args.mode, "temperature": w.temperature,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (W_lm exceeds the 129 MB L2), no flush"},
+        "committed_tokens_per_s": steps_per_s * tokens_per_step,
+        "mean_tokens_per_step": tokens_per_step,
+        "step_roofline": {"time_us": max(t_hbm, t_tc) * 1e6, "frac": max(t_hbm, t_tc) / step_s,
+                          "bound": "tensor" if tensor_bound else "hbm"},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": K * (3 if mode == wl.SAMPLE else 2),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(tv, w, inp, mode, K, Wm, args, device):
+    """Same metric through the host-pointer entry point, copies included."""
+    host = {k: v.cpu().pin_memory() for k, v in inp.items() if k != "W_lm"}
+    hl = host["draft_logits"] if mode == wl.SAMPLE else None
+    out = torch.empty(w.B, w.gamma + 1, dtype=torch.int32, pin_memory=True)
+    nacc = torch.empty(w.B, dtype=torch.int32, pin_memory=True)
+    ws = tv.alloc_workspace(w.B, w.gamma, w.d, w.V, inp["hidden"].dtype, mode, host=True,
+                            device=device)
+
+    def step(i):
+        tv.verify_host(host["hidden"], inp["W_lm"], host["draft_tokens"], hl, w.temperature,
+                       i, mode, out_tokens=out, n_accepted=nacc, workspace=ws)
+
+    for i in range(Wm):
+        step(i)
+    n = max(1, min(K, 2000))
+    t0 = time.perf_counter()
+    for i in range(n):
+        step(Wm + i)
+    dt = time.perf_counter() - t0
+    h2d = host["hidden"].numel() * host["hidden"].element_size() + host["draft_tokens"].numel() * 4
+    if hl is not None:
+        h2d += hl.numel() * hl.element_size()
+    d2h = out.numel() * 4 + nacc.numel() * 4
+    return {"value": n / dt, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n}
+
+
+# ---------------------------------------------------- reference arm --
+
+def run_reference(args, world, rank, local):
+    """The fp64 oracle on the host cores, on this arm's workload."""
+    if rank != 0:
+        return
+    from oracle import verify as ov
+    w = wl.get(args.workload)
+    mode = wl.SAMPLE if args.mode == "sample" else wl.GREEDY
+    device = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = wl.generate(w, args.seed, device=device)
+    h, W, x, dl = oracle_inputs(inp, mode)
+    # One full step, to size the per-step sample so the run fits the budget.
+    t0 = time.perf_counter()
+    ov.verify(h, W, x, dl, w.temperature, 0, mode)
+    t_full = time.perf_counter() - t0
+    n_total = args.steps + args.warmup
+    frac = min(1.0, REFERENCE_BUDGET_SECONDS / max(n_total * t_full, 1e-9))
+    Vs = max(1, int(w.V * frac))
+    Ws = W[:Vs]
+    xs = np.minimum(x, Vs - 1)
+    dls = dl[..., :Vs] if dl is not None else None
+    for i in range(args.warmup):
+        ov.verify(h, Ws, xs, dls, w.temperature, i, mode)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        ov.verify(h, Ws, xs, dls, w.temperature, args.warmup + k, mode)
+    dt = time.perf_counter() - t0
+    scale = Vs / w.V
+    value = args.steps * scale / dt
+    sample = (f"each step runs the fp64 oracle on the first {Vs} of {w.V} vocabulary rows "
+              f"(the oracle's cost is linear in V); value scaled by {Vs}/{w.V}")
+    line = {
+        "metric": METRIC, "value": value, "unit": "steps/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded; random-init LM head)",
+        "config": {"workload": args.workload, "B": w.B, "gamma": w.gamma, "d": w.d, "V": w.V,
+                   "mode": args.mode, "temperature": w.temperature},
+        "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "steps/s", "cores": host_cores(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_env()
+    if args.gpus != world and world > 1:
+        raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.impl == "reference":
+        run_reference(args, world, rank, local)
+    else:
+        run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,170 @@
+/*
+ * specdec_verify.h -- C ABI of the speculative-decoding verify step on one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * What one call computes ("推测解码", world.lapla.si/zh/specdec):
+ *   - section 先让小模型猜: the large model reads its LM-head weights once and
+ *     scores the gamma guessed positions plus one more. Row (b, i) of
+ *     `hidden` is the target state whose next-token distribution p_{b,i}
+ *     scores draft x_{b,i} (i < gamma); row (b, gamma) is the extra
+ *     position. Logits z = hidden . W_lm^T, p = softmax(z / T).
+ *   - section 通过的规则: draft x is kept iff r <= p(x)/q(x) with a uniform r
+ *     (tested as r*q(x) <= p(x)); q = softmax(draft_logits / T).
+ *   - section 留下对的，换掉错的: the first rejected draft j is replaced by a
+ *     token drawn from max(0, p_j - q_j) renormalised, and every later draft
+ *     is dropped; if all gamma drafts pass, a bonus token is drawn from
+ *     p_gamma. One call writes 1 .. gamma+1 tokens per sequence.
+ *   - greedy mode (maxstudionews.com article 1664, the verify paragraph):
+ *     keep drafts while each equals argmax z, and write the argmax at the
+ *     first mismatch (or at position gamma when all match).
+ *
+ * Random draws: Philox4x32-10 (Salmon et al., SC'11) with key = (seed low
+ * 32 bits, seed high 32 bits) and counter = (b, i, purpose, 0); k = word0
+ * >> 8; the acceptance uniform is r = (k+1)/2^24 (purpose 0) and the
+ * sampling uniform u = k/2^24 (purpose 1), drawn at the position where the
+ * replacement or bonus is written. The draw is the smallest token v with
+ * C_v > u*S, C the prefix sum of the weights in token-ID order and S its
+ * total; if S is 0 the draw falls back to p_j.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers unless stated otherwise, owned
+ *     by the caller, row-major and contiguous. The library allocates nothing
+ *     and keeps no state between calls (apart from a per-device cache of the
+ *     SM count and kernel attributes).
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and the call returns without synchronising, except where
+ *     stated.
+ *   - Return value: SPECDEC_OK (0) or a negative SPECDEC_ERR_* code.
+ *     Argument errors are detected on the host before anything is enqueued.
+ *     Errors found on the device (draft token out of [0, V), a kernel wait
+ *     that timed out) are written to a status word in the workspace; the
+ *     affected call then writes n_accepted = -1 and out_tokens = -1 for
+ *     every sequence. specdec_read_status() returns that word.
+ *   - Shapes: B >= 0 (B == 0 is a no-op), 1 <= gamma <= SPECDEC_MAX_GAMMA,
+ *     d >= 1 with d % 8 == 0 for bf16 (rows must be 16-byte aligned),
+ *     1 <= V, M = B*(gamma+1), and M*V < 2^31. Pointers to bf16 data must
+ *     be 16-byte aligned.
+ */
+#ifndef SPECDEC_VERIFY_H_
+#define SPECDEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPECDEC_MAX_GAMMA 32
+
+/* mode */
+#define SPECDEC_SAMPLE 0
+#define SPECDEC_GREEDY 1
+
+/* dtype of hidden, W_lm and draft_logits */
+#define SPECDEC_BF16 0
+#define SPECDEC_FP32 1
+
+/* status codes */
+#define SPECDEC_OK 0
+#define SPECDEC_ERR_INVALID_ARG (-1)   /* null pointer, bad enum, T <= 0 in sampling mode */
+#define SPECDEC_ERR_UNSUPPORTED (-2)   /* shape outside the limits above */
+#define SPECDEC_ERR_WORKSPACE (-3)     /* workspace NULL, misaligned or too small */
+#define SPECDEC_ERR_CUDA (-4)          /* a CUDA runtime/driver call failed */
+#define SPECDEC_ERR_TIMEOUT (-5)       /* a device-side wait ran out (status word) */
+#define SPECDEC_ERR_TOKEN_RANGE (-6)   /* a draft token outside [0, V) (status word) */
+
+/*
+ * Bytes of device workspace specdec_verify() needs for this shape. The
+ * workspace must be 256-byte aligned; its contents need no initialisation
+ * and are overwritten by every call. Calls that share a workspace must be
+ * ordered (same stream, or synchronised). Returns 0 for invalid shapes.
+ */
+size_t specdec_verify_workspace_size(int B, int gamma, int d, int V, int dtype, int mode);
+
+/*
+ * The verify step.
+ *   hidden       [B, gamma+1, d]  dtype   target hidden states (see above)
+ *   W_lm         [V, d]           dtype   LM-head weights, row v = token v
+ *   draft_tokens [B, gamma]       int32   the small model's guesses x
+ *   draft_logits [B, gamma, V]    dtype   the small model's logits for q;
+ *                                         may be NULL in greedy mode
+ *   temperature  T > 0 (sampling mode; ignored in greedy mode)
+ *   seed         Philox key (see above)
+ *   mode         SPECDEC_SAMPLE or SPECDEC_GREEDY
+ *   out_tokens   [B, gamma+1]     int32   written: kept drafts, then the
+ *                                         replacement or bonus token, then -1
+ *   n_accepted   [B]              int32   j = number of kept drafts, 0..gamma
+ *   workspace    device scratch of specdec_verify_workspace_size() bytes
+ */
+int specdec_verify(const void* hidden, const void* W_lm, const int32_t* draft_tokens,
+                   const void* draft_logits, int B, int gamma, int d, int V, int dtype,
+                   float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                   int32_t* n_accepted, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * specdec_verify() that also exposes its intermediates, for parity checks.
+ * Every extra pointer is an optional device buffer (NULL = not wanted):
+ *   logits_out [M, V] fp32  the target logits z
+ *   lse_p      [M]    fp32  log sum_v exp(z_v / T)           (sampling mode)
+ *   lse_q      [B*gamma]    log sum_v exp(draft_logit_v / T) (sampling mode)
+ *   p_x, q_x   [B*gamma]    p_i(x_i) and q_i(x_i)            (sampling mode)
+ *   argmax_out [M]   int32  argmax_v z (lowest v among equal maxima)
+ * Same results as specdec_verify() for the same inputs and seed.
+ */
+int specdec_verify_debug(const void* hidden, const void* W_lm, const int32_t* draft_tokens,
+                         const void* draft_logits, int B, int gamma, int d, int V, int dtype,
+                         float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                         int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                         void* stream, float* logits_out, float* lse_p, float* lse_q,
+                         float* p_x, float* q_x, int32_t* argmax_out);
+
+/*
+ * specdec_verify() with two caller-created CUDA events (cudaEvent_t)
+ * recorded on `stream` immediately before and after the LM-head kernel, so
+ * a caller can time that kernel inside a real step. Either may be NULL.
+ */
+int specdec_verify_timed(const void* hidden, const void* W_lm, const int32_t* draft_tokens,
+                         const void* draft_logits, int B, int gamma, int d, int V, int dtype,
+                         float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                         int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                         void* stream, void* lmhead_start_event, void* lmhead_end_event);
+
+/*
+ * End-to-end form: hidden, draft_tokens, draft_logits, out_tokens and
+ * n_accepted are HOST pointers (pinned memory gives asynchronous copies);
+ * W_lm and the workspace stay on the device. The call copies the inputs in,
+ * runs the step and copies the outputs back on `stream`, then synchronises
+ * that stream before returning. Workspace: specdec_verify_host_workspace_size().
+ */
+size_t specdec_verify_host_workspace_size(int B, int gamma, int d, int V, int dtype, int mode);
+int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t* draft_tokens_host,
+                        const void* draft_logits_host, int B, int gamma, int d, int V, int dtype,
+                        float temperature, uint64_t seed, int mode, int32_t* out_tokens_host,
+                        int32_t* n_accepted_host, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/*
+ * Reads the device status word of a workspace after synchronising `stream`:
+ * SPECDEC_OK, SPECDEC_ERR_TIMEOUT or SPECDEC_ERR_TOKEN_RANGE of the last
+ * call that used it. *status receives the value; the return code reports
+ * the read itself.
+ */
+int specdec_read_status(const void* workspace, void* stream, int32_t* status);
+
+/*
+ * The library's own uniforms, for checking them against another
+ * implementation: out[b*n_pos + i] = r (purpose 0) or u (purpose 1) for
+ * sequence b < B and position i < n_pos. `out` is a device fp32 buffer.
+ */
+int specdec_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose, float* out,
+                            void* stream);
+
+/* A static, human-readable name for a status code. */
+const char* specdec_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECDEC_VERIFY_H_ */

@@ -1,0 +1,142 @@
+"""Speculative-decoding verify step on one GB300 (sm_103a).
+
+The compute lives in libspecdec_verify.so (C ABI: include/specdec_verify.h);
+this package only marshals torch tensors into that ABI. See ``verify`` for
+the call a user makes.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _binding as _b
+from ._binding import (SPECDEC_BF16, SPECDEC_FP32, SPECDEC_GREEDY, SPECDEC_MAX_GAMMA,
+                       SPECDEC_SAMPLE, SpecdecError, status_string)
+
+SAMPLE = SPECDEC_SAMPLE
+GREEDY = SPECDEC_GREEDY
+
+_DTYPES = {torch.bfloat16: SPECDEC_BF16, torch.float32: SPECDEC_FP32}
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def _shape(hidden, W_lm):
+    B, g1, d = hidden.shape
+    V = W_lm.shape[0]
+    return B, g1 - 1, d, V
+
+
+def _check_inputs(hidden, W_lm, draft_tokens, draft_logits, mode, device_kind):
+    if hidden.dtype not in _DTYPES or W_lm.dtype != hidden.dtype:
+        raise TypeError("hidden and W_lm must both be bfloat16 or both float32")
+    if draft_tokens.dtype != torch.int32:
+        raise TypeError("draft_tokens must be int32")
+    if mode == SAMPLE and (draft_logits is None or draft_logits.dtype != hidden.dtype):
+        raise TypeError("sampling mode needs draft_logits in the dtype of hidden")
+    for t in (hidden, W_lm, draft_tokens, draft_logits):
+        if t is None:
+            continue
+        if not t.is_contiguous():
+            raise ValueError("all tensors must be contiguous")
+        if device_kind == "cuda" and not t.is_cuda:
+            raise ValueError("specdec_verify takes CUDA tensors")
+
+
+def workspace_bytes(B, gamma, d, V, dtype=torch.bfloat16, mode=SAMPLE, host=False) -> int:
+    fn = _b.specdec_verify_host_workspace_size if host else _b.specdec_verify_workspace_size
+    return fn(B, gamma, d, V, _DTYPES[dtype], mode)
+
+
+def alloc_workspace(B, gamma, d, V, dtype=torch.bfloat16, mode=SAMPLE, host=False, device=None):
+    n = workspace_bytes(B, gamma, d, V, dtype, mode, host)
+    if n == 0:
+        raise SpecdecError(_b.SPECDEC_ERR_UNSUPPORTED, "workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def verify(hidden, W_lm, draft_tokens, draft_logits, temperature=1.0, seed=0, mode=SAMPLE,
+           out_tokens=None, n_accepted=None, workspace=None, stream=None, debug=None,
+           events=None):
+    """One verify step (see include/specdec_verify.h for the contract).
+
+    hidden [B, gamma+1, d], W_lm [V, d] (bf16 or fp32), draft_tokens
+    [B, gamma] int32, draft_logits [B, gamma, V] (None allowed in greedy
+    mode). Returns (out_tokens [B, gamma+1] int32, n_accepted [B] int32).
+    `debug` may be a dict of preallocated CUDA tensors with keys logits,
+    lse_p, lse_q, p_x, q_x, argmax; `events` a (start, end) pair of
+    torch.cuda.Event recorded around the LM-head kernel.
+    """
+    _check_inputs(hidden, W_lm, draft_tokens, draft_logits, mode, "cuda")
+    B, gamma, d, V = _shape(hidden, W_lm)
+    dev = hidden.device
+    if out_tokens is None:
+        out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_workspace(B, gamma, d, V, hidden.dtype, mode, device=dev)
+    core = (_ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(draft_logits), B, gamma, d, V,
+            _DTYPES[hidden.dtype], float(temperature), int(seed) & (2 ** 64 - 1), int(mode),
+            _ptr(out_tokens), _ptr(n_accepted), _ptr(workspace), workspace.numel(),
+            _stream_ptr(stream))
+    if debug is not None:
+        rc = _b.specdec_verify_debug(*core, *(_ptr(debug.get(k)) for k in
+                                              ("logits", "lse_p", "lse_q", "p_x", "q_x", "argmax")))
+    elif events is not None:
+        rc = _b.specdec_verify_timed(*core, int(events[0].cuda_event), int(events[1].cuda_event))
+    else:
+        rc = _b.specdec_verify(*core)
+    _b._check(rc, "specdec_verify")
+    return out_tokens, n_accepted
+
+
+def verify_host(hidden, W_lm, draft_tokens, draft_logits, temperature=1.0, seed=0, mode=SAMPLE,
+                out_tokens=None, n_accepted=None, workspace=None, stream=None):
+    """End-to-end verify step from host (ideally pinned) CPU tensors.
+
+    W_lm and the workspace are CUDA tensors; the other inputs and both
+    outputs live in host memory. Returns after the step's outputs are back.
+    """
+    _check_inputs(hidden, W_lm, draft_tokens, draft_logits, mode, "host")
+    if not W_lm.is_cuda or hidden.is_cuda:
+        raise ValueError("verify_host takes W_lm on the device and the step's tensors on the host")
+    B, gamma, d, V = _shape(hidden, W_lm)
+    if out_tokens is None:
+        out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, pin_memory=True)
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, pin_memory=True)
+    if workspace is None:
+        workspace = alloc_workspace(B, gamma, d, V, hidden.dtype, mode, host=True,
+                                    device=W_lm.device)
+    rc = _b.specdec_verify_host(_ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(draft_logits),
+                                B, gamma, d, V, _DTYPES[hidden.dtype], float(temperature),
+                                int(seed) & (2 ** 64 - 1), int(mode), _ptr(out_tokens),
+                                _ptr(n_accepted), _ptr(workspace), workspace.numel(),
+                                _stream_ptr(stream))
+    _b._check(rc, "specdec_verify_host")
+    return out_tokens, n_accepted
+
+
+def read_status(workspace, stream=None) -> int:
+    """The device status word of the last call that used `workspace`."""
+    return _b.specdec_read_status(_ptr(workspace), _stream_ptr(stream))
+
+
+def philox_uniforms(seed, B, n_pos, purpose, device="cuda", stream=None):
+    """The library's r (purpose 0) or u (purpose 1) uniforms, [B, n_pos] fp32."""
+    out = torch.empty(B, n_pos, dtype=torch.float32, device=device)
+    rc = _b.specdec_philox_uniforms(int(seed) & (2 ** 64 - 1), B, n_pos, purpose, _ptr(out),
+                                    _stream_ptr(stream))
+    _b._check(rc, "specdec_philox_uniforms")
+    return out
+
+
+__all__ = ["verify", "verify_host", "alloc_workspace", "workspace_bytes", "read_status",
+           "philox_uniforms", "status_string", "SpecdecError", "SAMPLE", "GREEDY"]

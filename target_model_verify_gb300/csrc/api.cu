@@ -1,0 +1,381 @@
+// C ABI of the verify step: argument checks, workspace plan, tensor maps
+// and the stream-ordered launch sequence
+//   LM-head scoring (+ softmax/argmax partials)  ->  acceptance scan
+//   ->  residual / bonus draw (sampling mode only).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "kernels.h"
+
+using namespace specdec;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+struct Plan {
+  int M, P, nchunks;
+  size_t off_sel, off_counters, off_pp, off_pq, off_z, off_chunks, total;
+};
+
+// Checks the shape; returns SPECDEC_OK or an error code.
+int check_shape(int B, int gamma, int d, int V, int dtype, int mode) {
+  if (dtype != SPECDEC_BF16 && dtype != SPECDEC_FP32) return SPECDEC_ERR_INVALID_ARG;
+  if (mode != SPECDEC_SAMPLE && mode != SPECDEC_GREEDY) return SPECDEC_ERR_INVALID_ARG;
+  if (B < 0 || gamma < 1 || gamma > SPECDEC_MAX_GAMMA || d < 1 || V < 1)
+    return SPECDEC_ERR_UNSUPPORTED;
+  if (dtype == SPECDEC_BF16 && d % 8 != 0) return SPECDEC_ERR_UNSUPPORTED;
+  const long long M = (long long)B * (gamma + 1);
+  if (M * (long long)V >= (1ll << 31)) return SPECDEC_ERR_UNSUPPORTED;
+  if ((M + 15) / 16 > 65535) return SPECDEC_ERR_UNSUPPORTED;
+  return SPECDEC_OK;
+}
+
+Plan make_plan(int B, int gamma, int d, int V, int dtype, int mode) {
+  (void)d;
+  (void)dtype;
+  Plan p;
+  p.M = B * (gamma + 1);
+  p.P = (V + kBlockV - 1) / kBlockV;
+  p.nchunks = (V + kChunkV - 1) / kChunkV;
+  const bool sample = mode == SPECDEC_SAMPLE;
+  size_t off = align_up(sizeof(WsHeader));
+  p.off_sel = off;
+  off = align_up(off + sizeof(SelectedRow) * (size_t)B);
+  p.off_counters = off;
+  off = align_up(off + sizeof(int) * (size_t)B);
+  p.off_pp = off;
+  off = align_up(off + sizeof(PartialP) * (size_t)p.M * p.P);
+  p.off_pq = off;
+  if (sample) off = align_up(off + sizeof(PartialQ) * (size_t)B * gamma * p.P);
+  p.off_z = off;
+  if (sample) off = align_up(off + sizeof(float) * (size_t)p.M * V);
+  p.off_chunks = off;
+  if (sample) off = align_up(off + sizeof(float) * (size_t)B * p.nchunks);
+  p.total = off;
+  return p;
+}
+
+int num_sms_current() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (dev < 0 || dev >= 64) return -1;
+  if (cache[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    cache[dev] = n;
+  }
+  return cache[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] as a 2-D tensor map with a
+// {64, box_rows} box and the 128-byte swizzle; out-of-range rows read 0.
+bool encode_bf16_rows(CUtensorMap* map, const void* base, int rows, int cols, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  const cuuint32_t box[2] = {(cuuint32_t)kBlockK, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct Extras {
+  float* logits_out = nullptr;
+  float* lse_p = nullptr;
+  float* lse_q = nullptr;
+  float* p_x = nullptr;
+  float* q_x = nullptr;
+  int32_t* argmax_out = nullptr;
+  cudaEvent_t ev0 = nullptr;
+  cudaEvent_t ev1 = nullptr;
+};
+
+int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
+                const void* draft_logits, int B, int gamma, int d, int V, int dtype, float T,
+                uint64_t seed, int mode, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
+                size_t workspace_bytes, void* stream_ptr, const Extras& ex) {
+  int rc = check_shape(B, gamma, d, V, dtype, mode);
+  if (rc != SPECDEC_OK) return rc;
+  const bool sample = mode == SPECDEC_SAMPLE;
+  if (!hidden || !W || !draft_tokens || !out_tokens || !n_accepted) return SPECDEC_ERR_INVALID_ARG;
+  if (sample && (!draft_logits || !(T > 0.f) || !std::isfinite(T))) return SPECDEC_ERR_INVALID_ARG;
+  if (dtype == SPECDEC_BF16 &&
+      (((uintptr_t)hidden & 15u) != 0 || ((uintptr_t)W & 15u) != 0))
+    return SPECDEC_ERR_INVALID_ARG;
+  if (B == 0) return SPECDEC_OK;
+  const Plan pl = make_plan(B, gamma, d, V, dtype, mode);
+  if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || workspace_bytes < pl.total)
+    return SPECDEC_ERR_WORKSPACE;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SPECDEC_ERR_CUDA;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  SelectedRow* sel = reinterpret_cast<SelectedRow*>(ws + pl.off_sel);
+  int* counters = reinterpret_cast<int*>(ws + pl.off_counters);
+  PartialP* pp = reinterpret_cast<PartialP*>(ws + pl.off_pp);
+  PartialQ* pq = reinterpret_cast<PartialQ*>(ws + pl.off_pq);
+  float* z = ex.logits_out ? ex.logits_out : (sample ? reinterpret_cast<float*>(ws + pl.off_z) : nullptr);
+  float* chunk_sums = reinterpret_cast<float*>(ws + pl.off_chunks);
+  const float c = sample ? kLog2e / T : kLog2e;
+
+  // The status word is cleared with the first operation of the call.
+  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+
+  EpiParams ep;
+  ep.M = pl.M;
+  ep.V = V;
+  ep.gamma = gamma;
+  ep.P = pl.P;
+  ep.c = c;
+  ep.sample = sample ? 1 : 0;
+  ep.want_argmax = (!sample || ex.argmax_out) ? 1 : 0;
+  ep.zout = z;
+  ep.dl = draft_logits;
+  ep.pp = pp;
+  ep.pq = pq;
+
+  if (ex.ev0 && cudaEventRecord(ex.ev0, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  cudaError_t e;
+  if (dtype == SPECDEC_BF16) {
+    const TcGeometry g = tc_geometry(pl.M);
+    CUtensorMap tw, th;
+    if (!encode_bf16_rows(&tw, W, V, d, kBlockV) || !encode_bf16_rows(&th, hidden, pl.M, d, g.BT))
+      return SPECDEC_ERR_CUDA;
+    TcLaunch L;
+    L.tmap_w = &tw;
+    L.tmap_h = &th;
+    L.M = pl.M;
+    L.V = V;
+    L.d = d;
+    L.gamma = gamma;
+    L.BT = g.BT;
+    L.n_tt = g.n_tt;
+    L.status = status;
+    L.ep = ep;
+    e = launch_lmhead_tc(L, nsm, stream);
+  } else {
+    e = launch_lmhead_f32(static_cast<const float*>(hidden), static_cast<const float*>(W), d, ep,
+                          stream);
+  }
+  if (e != cudaSuccess) return SPECDEC_ERR_CUDA;
+  if (ex.ev1 && cudaEventRecord(ex.ev1, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+
+  AcceptLaunch A;
+  A.B = B;
+  A.gamma = gamma;
+  A.V = V;
+  A.P = pl.P;
+  A.mode = mode;
+  A.dl_bf16 = dtype == SPECDEC_BF16;
+  A.c = c;
+  A.seed = seed;
+  A.pp = pp;
+  A.pq = pq;
+  A.z = z;
+  A.dl = draft_logits;
+  A.draft_tokens = draft_tokens;
+  A.out_tokens = out_tokens;
+  A.n_accepted = n_accepted;
+  A.sel = sel;
+  A.counters = counters;
+  A.status = status;
+  A.lse_p = ex.lse_p;
+  A.lse_q = ex.lse_q;
+  A.p_x = ex.p_x;
+  A.q_x = ex.q_x;
+  A.argmax_out = ex.argmax_out;
+  if (launch_accept(A, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+
+  if (sample) {
+    SampleLaunch S;
+    S.B = B;
+    S.gamma = gamma;
+    S.V = V;
+    S.nchunks = pl.nchunks;
+    S.dl_bf16 = dtype == SPECDEC_BF16;
+    S.c = c;
+    S.seed = seed;
+    S.z = z;
+    S.dl = draft_logits;
+    S.sel = sel;
+    S.chunk_sums = chunk_sums;
+    S.counters = counters;
+    S.out_tokens = out_tokens;
+    if (launch_sample(S, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  }
+  return SPECDEC_OK;
+}
+
+size_t host_staging_bytes(int B, int gamma, int d, int V, int dtype, int mode) {
+  const size_t e = dtype == SPECDEC_BF16 ? 2 : 4;
+  const size_t M = (size_t)B * (gamma + 1);
+  size_t n = align_up(M * d * e);                                   // hidden
+  n += align_up((size_t)B * gamma * 4);                             // draft tokens
+  if (mode == SPECDEC_SAMPLE) n += align_up((size_t)B * gamma * V * e);   // draft logits
+  n += align_up(M * 4) + align_up((size_t)B * 4);                   // outputs
+  return n;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t specdec_verify_workspace_size(int B, int gamma, int d, int V, int dtype, int mode) {
+  if (check_shape(B, gamma, d, V, dtype, mode) != SPECDEC_OK) return 0;
+  return make_plan(B, gamma, d, V, dtype, mode).total;
+}
+
+int specdec_verify(const void* hidden, const void* W_lm, const int32_t* draft_tokens,
+                   const void* draft_logits, int B, int gamma, int d, int V, int dtype,
+                   float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                   int32_t* n_accepted, void* workspace, size_t workspace_bytes, void* stream) {
+  return verify_impl(hidden, W_lm, draft_tokens, draft_logits, B, gamma, d, V, dtype, temperature,
+                     seed, mode, out_tokens, n_accepted, workspace, workspace_bytes, stream,
+                     Extras());
+}
+
+int specdec_verify_debug(const void* hidden, const void* W_lm, const int32_t* draft_tokens,
+                         const void* draft_logits, int B, int gamma, int d, int V, int dtype,
+                         float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                         int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                         void* stream, float* logits_out, float* lse_p, float* lse_q, float* p_x,
+                         float* q_x, int32_t* argmax_out) {
+  Extras ex;
+  ex.logits_out = logits_out;
+  ex.lse_p = lse_p;
+  ex.lse_q = lse_q;
+  ex.p_x = p_x;
+  ex.q_x = q_x;
+  ex.argmax_out = argmax_out;
+  return verify_impl(hidden, W_lm, draft_tokens, draft_logits, B, gamma, d, V, dtype, temperature,
+                     seed, mode, out_tokens, n_accepted, workspace, workspace_bytes, stream, ex);
+}
+
+int specdec_verify_timed(const void* hidden, const void* W_lm, const int32_t* draft_tokens,
+                         const void* draft_logits, int B, int gamma, int d, int V, int dtype,
+                         float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                         int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                         void* stream, void* lmhead_start_event, void* lmhead_end_event) {
+  Extras ex;
+  ex.ev0 = static_cast<cudaEvent_t>(lmhead_start_event);
+  ex.ev1 = static_cast<cudaEvent_t>(lmhead_end_event);
+  return verify_impl(hidden, W_lm, draft_tokens, draft_logits, B, gamma, d, V, dtype, temperature,
+                     seed, mode, out_tokens, n_accepted, workspace, workspace_bytes, stream, ex);
+}
+
+size_t specdec_verify_host_workspace_size(int B, int gamma, int d, int V, int dtype, int mode) {
+  const size_t base = specdec_verify_workspace_size(B, gamma, d, V, dtype, mode);
+  if (base == 0) return 0;
+  return base + host_staging_bytes(B, gamma, d, V, dtype, mode);
+}
+
+int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t* draft_tokens_host,
+                        const void* draft_logits_host, int B, int gamma, int d, int V, int dtype,
+                        float temperature, uint64_t seed, int mode, int32_t* out_tokens_host,
+                        int32_t* n_accepted_host, void* workspace, size_t workspace_bytes,
+                        void* stream_ptr) {
+  int rc = check_shape(B, gamma, d, V, dtype, mode);
+  if (rc != SPECDEC_OK) return rc;
+  const bool sample = mode == SPECDEC_SAMPLE;
+  if (!hidden_host || !W_lm || !draft_tokens_host || !out_tokens_host || !n_accepted_host)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (sample && !draft_logits_host) return SPECDEC_ERR_INVALID_ARG;
+  if (B == 0) return SPECDEC_OK;
+  const size_t base = specdec_verify_workspace_size(B, gamma, d, V, dtype, mode);
+  const size_t need = base + host_staging_bytes(B, gamma, d, V, dtype, mode);
+  if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || workspace_bytes < need)
+    return SPECDEC_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  const size_t e = dtype == SPECDEC_BF16 ? 2 : 4;
+  const size_t M = (size_t)B * (gamma + 1);
+  char* p = static_cast<char*>(workspace) + base;
+  void* d_hidden = p;
+  p += align_up(M * d * e);
+  int32_t* d_tokens = reinterpret_cast<int32_t*>(p);
+  p += align_up((size_t)B * gamma * 4);
+  void* d_logits = nullptr;
+  if (sample) {
+    d_logits = p;
+    p += align_up((size_t)B * gamma * V * e);
+  }
+  int32_t* d_out = reinterpret_cast<int32_t*>(p);
+  p += align_up(M * 4);
+  int32_t* d_nacc = reinterpret_cast<int32_t*>(p);
+
+  if (cudaMemcpyAsync(d_hidden, hidden_host, M * d * e, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
+      cudaMemcpyAsync(d_tokens, draft_tokens_host, (size_t)B * gamma * 4, cudaMemcpyHostToDevice,
+                      stream) != cudaSuccess)
+    return SPECDEC_ERR_CUDA;
+  if (sample && cudaMemcpyAsync(d_logits, draft_logits_host, (size_t)B * gamma * V * e,
+                                cudaMemcpyHostToDevice, stream) != cudaSuccess)
+    return SPECDEC_ERR_CUDA;
+  rc = verify_impl(d_hidden, W_lm, d_tokens, d_logits, B, gamma, d, V, dtype, temperature, seed,
+                   mode, d_out, d_nacc, workspace, base, stream_ptr, Extras());
+  if (rc != SPECDEC_OK) return rc;
+  if (cudaMemcpyAsync(out_tokens_host, d_out, M * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
+      cudaMemcpyAsync(n_accepted_host, d_nacc, (size_t)B * 4, cudaMemcpyDeviceToHost, stream) !=
+          cudaSuccess)
+    return SPECDEC_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  return SPECDEC_OK;
+}
+
+int specdec_read_status(const void* workspace, void* stream, int32_t* status) {
+  if (!workspace || !status) return SPECDEC_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  if (cudaMemcpy(status, workspace, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPECDEC_ERR_CUDA;
+  return SPECDEC_OK;
+}
+
+int specdec_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose, float* out,
+                            void* stream) {
+  if (!out || B < 0 || n_pos < 0 || (purpose != 0 && purpose != 1)) return SPECDEC_ERR_INVALID_ARG;
+  if ((long long)B * n_pos >= (1ll << 31)) return SPECDEC_ERR_UNSUPPORTED;
+  if (B == 0 || n_pos == 0) return SPECDEC_OK;
+  return launch_philox_uniforms(seed, B, n_pos, purpose, out, static_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? SPECDEC_OK
+             : SPECDEC_ERR_CUDA;
+}
+
+const char* specdec_status_string(int status) {
+  switch (status) {
+    case SPECDEC_OK: return "ok";
+    case SPECDEC_ERR_INVALID_ARG: return "invalid argument";
+    case SPECDEC_ERR_UNSUPPORTED: return "unsupported shape";
+    case SPECDEC_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+    case SPECDEC_ERR_CUDA: return "CUDA error";
+    case SPECDEC_ERR_TIMEOUT: return "device-side wait timed out";
+    case SPECDEC_ERR_TOKEN_RANGE: return "draft token outside [0, V)";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,76 @@
+// Host-side launch interface between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace specdec {
+
+// LM-head scoring on the tensor cores (bf16 inputs): logits z = hidden.W^T
+// for every token row, with the per-tile softmax / argmax partials and the
+// draft-logit partials fused into the epilogue.
+struct TcLaunch {
+  const CUtensorMap* tmap_w;     // W_lm [V, d], box {64, 128}, 128B swizzle
+  const CUtensorMap* tmap_h;     // hidden [M, d], box {64, BT}, 128B swizzle
+  int M, V, d, gamma;
+  int BT;                        // token rows per tile: multiple of 16, <= 256
+  int n_tt;                      // token tiles
+  int* status;
+  EpiParams ep;
+};
+cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream);
+
+// The same scoring for fp32 inputs on the CUDA cores.
+cudaError_t launch_lmhead_f32(const float* hidden, const float* W, int d, const EpiParams& ep,
+                              cudaStream_t stream);
+
+// Combine the partials, apply the acceptance rule, write the kept prefix.
+struct AcceptLaunch {
+  int B, gamma, V, P, mode, dl_bf16;
+  float c;                       // log2(e) / T
+  uint64_t seed;
+  const PartialP* pp;
+  const PartialQ* pq;
+  const float* z;
+  const void* dl;
+  const int32_t* draft_tokens;
+  int32_t* out_tokens;
+  int32_t* n_accepted;
+  SelectedRow* sel;
+  int* counters;
+  int* status;
+  float* lse_p;
+  float* lse_q;
+  float* p_x;
+  float* q_x;
+  int32_t* argmax_out;
+};
+cudaError_t launch_accept(const AcceptLaunch& L, cudaStream_t stream);
+
+// Residual / bonus draw for every sequence (sampling mode).
+struct SampleLaunch {
+  int B, gamma, V, nchunks, dl_bf16;
+  float c;
+  uint64_t seed;
+  const float* z;
+  const void* dl;
+  const SelectedRow* sel;
+  float* chunk_sums;
+  int* counters;
+  int32_t* out_tokens;
+};
+cudaError_t launch_sample(const SampleLaunch& L, cudaStream_t stream);
+
+cudaError_t launch_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose, float* out,
+                                   cudaStream_t stream);
+
+// Tile geometry of the tensor-core path, shared by the planner and launcher.
+struct TcGeometry {
+  int BT, n_tt, stages, stage_bytes, tmem_cols, smem_bytes;
+};
+TcGeometry tc_geometry(int M);
+
+}  // namespace specdec

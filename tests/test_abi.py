@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads and exports what its header declares, and
+its host-side argument checks answer before anything reaches a GPU (CPU)."""
+import ctypes
+
+import pytest
+
+from target_model_verify_gb300 import _binding as b
+from target_model_verify_gb300 import build as libbuild
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return b.lib()
+
+
+def test_exports_every_header_symbol(lib):
+    names = b.header_functions()
+    assert len(names) >= 9
+    for name in names:
+        assert hasattr(lib, name), name
+    assert set(names) == set(b._SIGNATURES)
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert b.status_string(code) not in ("", "unknown status")
+    assert b.status_string(-99) == "unknown status"
+
+
+def test_workspace_size(lib):
+    n = b.specdec_verify_workspace_size(1, 4, 4096, 128256, b.SPECDEC_BF16, b.SPECDEC_SAMPLE)
+    # holds at least the fp32 logits of the 5 rows
+    assert n >= 5 * 128256 * 4
+    g = b.specdec_verify_workspace_size(1, 4, 4096, 128256, b.SPECDEC_BF16, b.SPECDEC_GREEDY)
+    assert 0 < g < n
+    assert b.specdec_verify_workspace_size(1, 0, 4096, 128256, 0, 0) == 0      # gamma = 0
+    assert b.specdec_verify_workspace_size(1, 33, 4096, 128256, 0, 0) == 0     # gamma > max
+    assert b.specdec_verify_workspace_size(1, 4, 4090, 128256, 0, 0) == 0      # d % 8 != 0
+    assert b.specdec_verify_workspace_size(1, 4, 64, 512, 7, 0) == 0          # bad dtype
+    assert b.specdec_verify_workspace_size(1, 4, 64, 512, 0, 3) == 0          # bad mode
+    assert b.specdec_verify_workspace_size(20000, 32, 64, 128256, 0, 0) == 0  # M*V >= 2^31
+    h = b.specdec_verify_host_workspace_size(1, 4, 4096, 128256, 0, 0)
+    assert h > n
+
+
+def _call(B=1, gamma=4, d=64, V=512, dtype=1, T=1.0, mode=0, ptr=4096, ws=256, ws_bytes=1 << 30,
+          dl=4096):
+    # Fake but aligned addresses: every check below fails before any access.
+    return b.specdec_verify(ptr, ptr, ptr, dl, B, gamma, d, V, dtype, T, 0, mode, ptr, ptr,
+                            ws, ws_bytes, None)
+
+
+def test_host_side_argument_errors(lib):
+    assert _call(ptr=0) == b.SPECDEC_ERR_INVALID_ARG
+    assert _call(dl=0) == b.SPECDEC_ERR_INVALID_ARG                 # sampling needs q
+    assert _call(T=0.0) == b.SPECDEC_ERR_INVALID_ARG
+    assert _call(T=-1.0) == b.SPECDEC_ERR_INVALID_ARG
+    assert _call(T=float("nan")) == b.SPECDEC_ERR_INVALID_ARG
+    assert _call(gamma=0) == b.SPECDEC_ERR_UNSUPPORTED
+    assert _call(gamma=33) == b.SPECDEC_ERR_UNSUPPORTED
+    assert _call(dtype=0, d=60) == b.SPECDEC_ERR_UNSUPPORTED
+    assert _call(dtype=0, ptr=4098) == b.SPECDEC_ERR_INVALID_ARG     # bf16 needs 16B alignment
+    assert _call(ws=0) == b.SPECDEC_ERR_WORKSPACE
+    assert _call(ws=300) == b.SPECDEC_ERR_WORKSPACE                  # misaligned
+    assert _call(ws_bytes=16) == b.SPECDEC_ERR_WORKSPACE
+    assert _call(B=0) == b.SPECDEC_OK                                # empty batch: no-op
+    assert _call(mode=5) == b.SPECDEC_ERR_INVALID_ARG
+    # greedy mode does not need draft logits or a temperature
+    assert _call(mode=1, dl=0, T=0.0, ws=0) == b.SPECDEC_ERR_WORKSPACE
+
+
+def test_philox_argument_errors(lib):
+    assert b.specdec_philox_uniforms(0, 1, 1, 2, 4096, None) == b.SPECDEC_ERR_INVALID_ARG
+    assert b.specdec_philox_uniforms(0, 1, 1, 0, 0, None) == b.SPECDEC_ERR_INVALID_ARG
+    assert b.specdec_philox_uniforms(0, 0, 5, 0, 4096, None) == b.SPECDEC_OK
+
+
+def test_read_status_argument_errors(lib):
+    st = ctypes.c_int32(0)
+    assert lib.specdec_read_status(None, None, ctypes.byref(st)) == b.SPECDEC_ERR_INVALID_ARG

@@ -1,0 +1,229 @@
+"""GPU parity: the C-ABI library against the fp64 oracle on seeded inputs.
+
+Every test calls the library through its C ABI (ctypes) on cuda:0 and
+compares with the oracle on byte-identical inputs, under the rule stated in
+tests/parity.py. Small cases cover several vocabulary tiles, a ragged
+vocabulary tail, several token tiles and the degenerate cases; the
+full-size workloads are checked on every sequence the oracle can afford and
+on structural invariants for the rest.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import verify as ov
+from target_model_verify_gb300 import workloads as wl
+
+from . import parity
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from target_model_verify_gb300 import build
+    build.build()
+    import target_model_verify_gb300  # noqa: F401  (fails loudly if the library is missing)
+    torch.cuda.init()
+
+
+def _gen(name, seed, **over):
+    w = wl.get(name, **over)
+    return w, wl.generate(w, seed, device=DEV)
+
+
+def _full_check(w, inp, seed, mode, rows=None):
+    T = w.temperature
+    out, nacc, dbg = parity.run_library(inp, T, seed, mode)
+    res = parity.run_oracle(inp, T, seed, mode, seq_ids=rows)
+    rep = parity.assert_tokens(out, nacc, res, mode, rows)
+    parity.assert_intermediates(dbg, res, mode, w.B, w.gamma, rows)
+    parity.check_structure(out, nacc, inp["draft_tokens"].cpu().numpy(), w.V)
+    return out, nacc, rep
+
+
+# ------------------------------------------------------------ Philox --
+
+def test_philox_uniforms_match_oracle():
+    import target_model_verify_gb300 as tv
+    from oracle import philox
+    seed = 0xDEADBEEF12345678
+    for purpose, fn in ((0, philox.accept_uniform), (1, philox.sample_uniform)):
+        got = tv.philox_uniforms(seed, 300, 33, purpose, device=DEV).cpu().double().numpy()
+        b = np.repeat(np.arange(300), 33).reshape(300, 33)
+        i = np.tile(np.arange(33), 300).reshape(300, 33)
+        np.testing.assert_array_equal(got, fn(seed, b, i))
+
+
+# ------------------------------------------------- small, several tiles --
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_tiny_fp32_sampling(seed):
+    w, inp = _gen("tiny_fp32", seed)
+    _full_check(w, inp, seed, ov.SAMPLE)
+
+
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+@pytest.mark.parametrize("B,gamma,d,V,T", [
+    (3, 4, 256, 1000, 0.8),     # ragged vocabulary tail (1000 = 7*128 + 104)
+    (2, 1, 64, 128, 1.0),       # one tile, gamma = 1
+    (60, 4, 128, 700, 1.3),     # M = 300: two token tiles of 160
+    (1, 32, 192, 2049, 0.5),    # gamma at its maximum, ragged tail
+    (7, 3, 8, 300, 1.0),        # d = 8: one zero-padded k-slice
+])
+def test_bf16_small_shapes(mode, B, gamma, d, V, T):
+    w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, temperature=T, sigma=0.4)
+    inp = wl.generate(w, 11 + B, device=DEV)
+    _full_check(w, inp, 5, mode)
+
+
+def test_fp32_small_shapes_greedy():
+    w = wl.get("tiny_fp32", B=5, gamma=3, d=40, V=777)
+    inp = wl.generate(w, 3, device=DEV)
+    _full_check(w, inp, 9, ov.GREEDY)
+    _full_check(w, inp, 9, ov.SAMPLE)
+
+
+# ------------------------------------------------------ full-size heads --
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+def test_llama3_8b_head(seed, mode):
+    w, inp = _gen("llama3_8b_head", seed)
+    _full_check(w, inp, seed, mode)
+
+
+@pytest.mark.parametrize("gamma", [1, 2, 3, 4, 6, 8])
+def test_gemma_e2b_head_gamma_sweep(gamma):
+    w, inp = _gen(f"gemma_e2b_head_g{gamma}", 0)
+    _full_check(w, inp, 0, ov.SAMPLE)
+
+
+@pytest.mark.parametrize("B", [4, 16, 64, 256])
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+def test_llama3_8b_head_batch_sweep(B, mode):
+    w, inp = _gen(f"llama3_8b_head_b{B}", 1)
+    rows = sorted(set([0, B // 3, B // 2, B - 1]))
+    _full_check(w, inp, 3, mode, rows=rows)
+
+
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+def test_head_70b(mode):
+    w, inp = _gen("head_70b_b32_g7", 2)
+    rows = [0, 7, 19, 31]
+    _full_check(w, inp, 4, mode, rows=rows)
+
+
+# ------------------------------------------------------------ behaviour --
+
+def test_deterministic_and_seed_sensitive():
+    w, inp = _gen("llama3_8b_head", 0, V=5000, d=512)
+    a = parity.run_library(inp, 1.0, 77, ov.SAMPLE)
+    b = parity.run_library(inp, 1.0, 77, ov.SAMPLE)
+    np.testing.assert_array_equal(a[0], b[0])
+    assert torch.equal(a[2]["logits"], b[2]["logits"])
+    assert torch.equal(a[2]["lse_p"], b[2]["lse_p"])
+
+
+def test_all_accepted_and_all_rejected():
+    """q == p keeps every draft (bonus written at position gamma); a draft
+    with p = 0 is always rejected and never comes back as the replacement."""
+    w = wl.get("llama3_8b_head", B=4, gamma=4, d=128, V=600, sigma=0.3)
+    inp = wl.generate(w, 21, device=DEV)
+    # draft logits equal to the target's own logits: q == p up to bf16 rounding
+    z = (inp["hidden"].float() @ inp["W_lm"].float().T)[:, :4]
+    inp_eq = dict(inp, draft_logits=z.to(torch.bfloat16).contiguous())
+    out, nacc, _ = parity.run_library(inp_eq, 1.0, 3, ov.SAMPLE)
+    res = parity.run_oracle(inp_eq, 1.0, 3, ov.SAMPLE)
+    parity.assert_tokens(out, nacc, res, ov.SAMPLE)
+    # strongly wrong drafts: q concentrated on a token the target gives ~0
+    zq = torch.full_like(inp["draft_logits"], -30.0)
+    x = torch.argmin(z, dim=-1).int()
+    zq.scatter_(2, x.long().unsqueeze(-1), 30.0)
+    inp_bad = dict(inp, draft_logits=zq.contiguous(), draft_tokens=x.contiguous())
+    out, nacc, _ = parity.run_library(inp_bad, 1.0, 3, ov.SAMPLE)
+    assert np.all(nacc == 0)
+    assert np.all(out[:, 0] != x[:, 0].cpu().numpy())
+    res = parity.run_oracle(inp_bad, 1.0, 3, ov.SAMPLE)
+    parity.assert_tokens(out, nacc, res, ov.SAMPLE)
+
+
+def test_greedy_ignores_temperature_and_draft_logits():
+    w, inp = _gen("llama3_8b_head", 4, V=3000, d=256)
+    a = parity.run_library(inp, 1.0, 1, ov.GREEDY, debug=False)
+    b = parity.run_library(dict(inp, draft_logits=None), 0.3, 99, ov.GREEDY, debug=False)
+    np.testing.assert_array_equal(a[0], b[0])
+
+
+def test_draft_token_out_of_range_sets_status():
+    import target_model_verify_gb300 as tv
+    w, inp = _gen("llama3_8b_head", 5, B=3, V=1000, d=128)
+    bad = inp["draft_tokens"].clone()
+    bad[1, 2] = w.V            # out of [0, V)
+    ws = tv.alloc_workspace(w.B, w.gamma, w.d, w.V, torch.bfloat16, ov.SAMPLE, device=DEV)
+    out, nacc = tv.verify(inp["hidden"], inp["W_lm"], bad, inp["draft_logits"], 1.0, 0,
+                          ov.SAMPLE, workspace=ws)
+    assert tv.read_status(ws) == tv._b.SPECDEC_ERR_TOKEN_RANGE
+    nacc = nacc.cpu().numpy()
+    assert nacc[1] == -1 and np.all(out[1].cpu().numpy() == -1)
+    assert nacc[0] >= 0 and nacc[2] >= 0
+    # the next good call on the same workspace clears the status
+    tv.verify(inp["hidden"], inp["W_lm"], inp["draft_tokens"], inp["draft_logits"], 1.0, 0,
+              ov.SAMPLE, workspace=ws)
+    assert tv.read_status(ws) == 0
+
+
+def test_empty_batch_is_a_noop():
+    import target_model_verify_gb300 as tv
+    w = wl.get("llama3_8b_head", B=1, V=256, d=64)
+    inp = wl.generate(w, 0, device=DEV)
+    h = inp["hidden"][:0]
+    out, nacc = tv.verify(h, inp["W_lm"], inp["draft_tokens"][:0], inp["draft_logits"][:0],
+                          1.0, 0, ov.SAMPLE,
+                          workspace=torch.empty(256, dtype=torch.uint8, device=DEV))
+    assert out.shape == (0, 5) and nacc.shape == (0,)
+
+
+def test_host_entry_point_matches_device_entry_point():
+    import target_model_verify_gb300 as tv
+    w, inp = _gen("llama3_8b_head", 6, B=2, V=4000, d=256)
+    dev_out, dev_nacc, _ = parity.run_library(inp, 1.0, 8, ov.SAMPLE, debug=False)
+    host = {k: v.cpu().pin_memory() for k, v in inp.items() if k != "W_lm"}
+    out, nacc = tv.verify_host(host["hidden"], inp["W_lm"], host["draft_tokens"],
+                               host["draft_logits"], 1.0, 8, ov.SAMPLE)
+    np.testing.assert_array_equal(out.numpy(), dev_out)
+    np.testing.assert_array_equal(nacc.numpy(), dev_nacc)
+
+
+def test_chi_square_committed_token_law():
+    """Distribution preservation on the GPU: over 2*10^5 draws the first
+    written token follows p0 and the kept fraction is sum min(p0, q0)
+    ("推测解码", sections 和大模型写的一样 and 接受率 α)."""
+    stats = pytest.importorskip("scipy.stats")
+    import target_model_verify_gb300 as tv
+    V, d, B, calls = 64, 64, 10000, 20
+    w = wl.get("llama3_8b_head", B=1, gamma=1, d=d, V=V, sigma=0.8, w_std=0.3)
+    base = wl.generate(w, 123, device=DEV)
+    hidden = base["hidden"].expand(B, -1, -1).contiguous()
+    dl = base["draft_logits"].expand(B, -1, -1).contiguous()
+    res1 = parity.run_oracle(base, 1.0, 0, ov.SAMPLE)
+    p0, _ = ov.softmax_t(res1.z[0, 0], 1.0)
+    q0, _ = ov.softmax_t(parity.to_f64(base["draft_logits"])[0, 0], 1.0)
+    rng = np.random.default_rng(5)
+    ws = tv.alloc_workspace(B, 1, d, V, torch.bfloat16, ov.SAMPLE, device=DEV)
+    counts = np.zeros(V)
+    kept = 0
+    for c in range(calls):
+        x = torch.as_tensor(rng.choice(V, size=(B, 1), p=q0), dtype=torch.int32, device=DEV)
+        out, nacc = tv.verify(hidden, base["W_lm"], x, dl, 1.0, 1000 + c, ov.SAMPLE,
+                              workspace=ws)
+        counts += np.bincount(out[:, 0].cpu().numpy(), minlength=V)
+        kept += int((nacc == 1).sum())
+    n = B * calls
+    assert stats.chisquare(counts, p0 * n).pvalue > 1e-4
+    alpha = np.minimum(p0, q0).sum()
+    assert abs(kept / n - alpha) < 4 * math.sqrt(alpha * (1 - alpha) / n)

@@ -40,7 +40,8 @@
  *     that timed out) are written to a status word in the workspace; the
  *     affected call then writes n_accepted = -1 and out_tokens = -1 for
  *     every sequence. specdec_read_status() returns that word.
- *   - Shapes: B >= 0 (B == 0 is a no-op), 1 <= gamma <= SPECDEC_MAX_GAMMA,
+ *   - Shapes: B >= 0 (B == 0 returns SPECDEC_OK and touches no pointer),
+ *     1 <= gamma <= SPECDEC_MAX_GAMMA,
  *     d >= 1 with d % 8 == 0 for bf16 (rows must be 16-byte aligned),
  *     1 <= V, M = B*(gamma+1), and M*V < 2^31. Pointers to bf16 data must
  *     be 16-byte aligned.

@@ -119,13 +119,13 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
                 size_t workspace_bytes, void* stream_ptr, const Extras& ex) {
   int rc = check_shape(B, gamma, d, V, dtype, mode);
   if (rc != SPECDEC_OK) return rc;
+  if (B == 0) return SPECDEC_OK;   // empty batch: nothing is read or written
   const bool sample = mode == SPECDEC_SAMPLE;
   if (!hidden || !W || !draft_tokens || !out_tokens || !n_accepted) return SPECDEC_ERR_INVALID_ARG;
   if (sample && (!draft_logits || !(T > 0.f) || !std::isfinite(T))) return SPECDEC_ERR_INVALID_ARG;
   if (dtype == SPECDEC_BF16 &&
       (((uintptr_t)hidden & 15u) != 0 || ((uintptr_t)W & 15u) != 0))
     return SPECDEC_ERR_INVALID_ARG;
-  if (B == 0) return SPECDEC_OK;
   const Plan pl = make_plan(B, gamma, d, V, dtype, mode);
   if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || workspace_bytes < pl.total)
     return SPECDEC_ERR_WORKSPACE;
@@ -301,11 +301,11 @@ int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t
                         void* stream_ptr) {
   int rc = check_shape(B, gamma, d, V, dtype, mode);
   if (rc != SPECDEC_OK) return rc;
+  if (B == 0) return SPECDEC_OK;
   const bool sample = mode == SPECDEC_SAMPLE;
   if (!hidden_host || !W_lm || !draft_tokens_host || !out_tokens_host || !n_accepted_host)
     return SPECDEC_ERR_INVALID_ARG;
   if (sample && !draft_logits_host) return SPECDEC_ERR_INVALID_ARG;
-  if (B == 0) return SPECDEC_OK;
   const size_t base = specdec_verify_workspace_size(B, gamma, d, V, dtype, mode);
   const size_t need = base + host_staging_bytes(B, gamma, d, V, dtype, mode);
   if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || workspace_bytes < need)

@@ -9,8 +9,9 @@ probability for a token, q the small model's (section 通过的规则).
 
 Row layout (the reading shared with the CUDA library): hidden[b, i] is the
 target state whose next-token distribution p_{b,i} scores draft x_{b,i} for
-i < gamma; hidden[b, gamma] is the extra position the same pass computes
-("check these 4, and compute the 5th"). draft_logits[b, i] gives q_{b,i}.
+i < gamma; hidden[b, gamma] is the extra position: the pass that checks
+the guesses also scores the position after the last one. draft_logits[b, i]
+gives q_{b,i}.
 
 Readings where the pages are silent (each is also the CUDA library's):
 

@@ -146,6 +146,36 @@ int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t
                         void* stream);
 
 /*
+ * specdec_verify() for callers that cannot allocate device memory. The
+ * source pages have no counterpart to this entry point: it exists because
+ * some callers cannot hand the library a workspace -- code running inside a
+ * host program that owns all device memory and gives its plug-ins no
+ * allocator, or a decode loop whose memory was planned up front, where a
+ * cudaMalloc would synchronise the device or fail against a caching
+ * allocator's reservation.
+ *
+ * Same arguments and results as specdec_verify(), minus the workspace: the
+ * scratch is a static device array of SPECDEC_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) that every GPU which loads the library holds until the process
+ * exits. Shapes whose specdec_verify_workspace_size() exceeds that are
+ * rejected with SPECDEC_ERR_WORKSPACE before anything is enqueued (one
+ * sequence fits at every head shape here, e.g. 2.6 MiB for the
+ * Llama-3-8B-shaped head, 9.4 MiB for the Gemma-E2B head at gamma = 8).
+ * The call allocates nothing. Its first call on each device looks up the
+ * array's device address (cudaGetSymbolAddress) with that device current;
+ * make that first call before any stream capture. All calls share the one
+ * array and each clears what must start at zero, but calls whose work
+ * overlaps on the GPU (different streams, or different host threads
+ * without ordering) race on it and must be serialised by the caller.
+ * specdec_read_status() does not apply: the status word lives in the array.
+ */
+#define SPECDEC_NOALLOC_SCRATCH_BYTES (16u << 20)
+int specdec_verify_noalloc(const void* hidden, const void* W_lm, const int32_t* draft_tokens,
+                           const void* draft_logits, int B, int gamma, int d, int V, int dtype,
+                           float temperature, uint64_t seed, int mode, int32_t* out_tokens,
+                           int32_t* n_accepted, void* stream);
+
+/*
  * Reads the device status word of a workspace after synchronising `stream`:
  * SPECDEC_OK, SPECDEC_ERR_TIMEOUT or SPECDEC_ERR_TOKEN_RANGE of the last
  * call that used it. *status receives the value; the return code reports

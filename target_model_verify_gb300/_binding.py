@@ -48,6 +48,7 @@ _SIGNATURES = {
     "specdec_read_status": (_i, [_vp, _vp, ctypes.POINTER(ctypes.c_int32)]),
     "specdec_philox_uniforms": (_i, [_u64, _i, _i, _i, _vp, _vp]),
     "specdec_status_string": (ctypes.c_char_p, [_i]),
+    "specdec_verify_noalloc": (_i, _CORE[:14] + [_vp]),
 }
 
 _lib = None
@@ -117,6 +118,11 @@ def specdec_verify_timed(*args) -> int:
 
 def specdec_verify_host(*args) -> int:
     return int(lib().specdec_verify_host(*args))
+
+
+def specdec_verify_noalloc(*args) -> int:
+    """The verify step with the library's static scratch (no workspace)."""
+    return int(lib().specdec_verify_noalloc(*args))
 
 
 def specdec_read_status(workspace_ptr: int, stream_ptr: int) -> int:

@@ -220,13 +220,19 @@ def run_ours(args, world, rank, local):
     t_wall0 = time.time()
     start.record()
     for k in range(K):
-        step(Wm + k, (ev0[k], ev1[k]))
+        step(Wm + k)
     end.record()
     torch.cuda.synchronize()
     t_wall1 = time.time()
     if world > 1:
         torch.distributed.barrier()
     elapsed_ms = start.elapsed_time(end)
+    # Second timed pass: the same K steps with events recorded around the
+    # LM-head kernel (an event between two kernels stops the next one from
+    # launching early, so the headline pass above runs without them).
+    for k in range(K):
+        step(Wm + k, (ev0[k], ev1[k]))
+    torch.cuda.synchronize()
     lm_ms = [a.elapsed_time(b) for a, b in zip(ev0, ev1)]
     if sampler:
         time.sleep(0.2)

@@ -43,7 +43,7 @@
  *   - Shapes: B >= 0 (B == 0 returns SPECDEC_OK and touches no pointer),
  *     1 <= gamma <= SPECDEC_MAX_GAMMA,
  *     d >= 1 with d % 8 == 0 for bf16 (rows must be 16-byte aligned),
- *     1 <= V, M = B*(gamma+1), and M*V < 2^31. Pointers to bf16 data must
+ *     1 <= V <= 2^22, M = B*(gamma+1), and M*V < 2^31. Pointers to bf16 data must
  *     be 16-byte aligned.
  */
 #ifndef SPECDEC_VERIFY_H_
@@ -159,8 +159,8 @@ int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t
  * (16 MiB) that every GPU which loads the library holds until the process
  * exits. Shapes whose specdec_verify_workspace_size() exceeds that are
  * rejected with SPECDEC_ERR_WORKSPACE before anything is enqueued (one
- * sequence fits at every head shape here, e.g. 2.6 MiB for the
- * Llama-3-8B-shaped head, 9.4 MiB for the Gemma-E2B head at gamma = 8).
+ * sequence fits at every head shape here, e.g. 6.6 MiB for the
+ * Llama-3-8B-shaped head, 13.4 MiB for the Gemma-E2B head at gamma = 8).
  * The call allocates nothing. Its first call on each device looks up the
  * array's device address (cudaGetSymbolAddress) with that device current;
  * make that first call before any stream capture. All calls share the one

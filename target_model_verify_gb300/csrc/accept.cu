@@ -16,6 +16,7 @@ namespace specdec {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kBatch = 8;
 
 template <typename DL>
 __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) {
@@ -30,18 +31,31 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
   const bool sample = a.mode == SPECDEC_SAMPLE;
   const int rows = g1 + (sample ? gamma : 0);
 
+  grid_dependency_wait();      // the LM-head kernel's records are complete
+  grid_launch_dependents();    // the sampler may start launching
+
   for (int r = warp; r < rows; r += kThreads / 32) {
     float m = -INFINITY, s = 0.f;
     if (r < g1) {
       const PartialP* row = a.pp + (size_t)(b * g1 + r) * a.P;
       float av = -INFINITY;
       int ai = 0x7fffffff;
-      for (int t = lane; t < a.P; t += 32) {
-        const PartialP x = row[t];
-        if (sample) softmax_merge(m, s, x.m, x.s, a.c);
-        if (argmax_better(x.amax_v, x.amax_i, av, ai)) {
-          av = x.amax_v;
-          ai = x.amax_i;
+      // Records t = lane, lane+32, ... folded in that order; kBatch loads
+      // are issued before their merges so they overlap in flight.
+      for (int base = lane; base < a.P; base += 32 * kBatch) {
+        PartialP x[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int t = base + 32 * u;
+          x[u] = t < a.P ? row[t] : PartialP{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (sample) softmax_merge(m, s, x[u].m, x[u].s, a.c);
+          if (argmax_better(x[u].amax_v, x[u].amax_i, av, ai)) {
+            av = x[u].amax_v;
+            ai = x[u].amax_i;
+          }
         }
       }
 #pragma unroll
@@ -60,9 +74,15 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
     } else {
       const int i = r - g1;
       const PartialQ* row = a.pq + ((size_t)b * gamma + i) * a.P;
-      for (int t = lane; t < a.P; t += 32) {
-        const PartialQ x = row[t];
-        softmax_merge(m, s, x.m, x.s, a.c);
+      for (int base = lane; base < a.P; base += 32 * kBatch) {
+        PartialQ x[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int t = base + 32 * u;
+          x[u] = t < a.P ? row[t] : PartialQ{-INFINITY, 0.f};
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) softmax_merge(m, s, x[u].m, x[u].s, a.c);
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
@@ -139,11 +159,17 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
 }  // namespace
 
 cudaError_t launch_accept(const AcceptLaunch& L, cudaStream_t stream) {
-  if (L.dl_bf16)
-    accept_kernel<__nv_bfloat16><<<L.B, kThreads, 0, stream>>>(L);
-  else
-    accept_kernel<float><<<L.B, kThreads, 0, stream>>>(L);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (L.dl_bf16) return cudaLaunchKernelEx(&cfg, accept_kernel<__nv_bfloat16>, L);
+  return cudaLaunchKernelEx(&cfg, accept_kernel<float>, L);
 }
 
 }  // namespace specdec

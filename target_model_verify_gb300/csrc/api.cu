@@ -20,14 +20,15 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 struct Plan {
   int M, P, nchunks;
-  size_t off_sel, off_counters, off_pp, off_pq, off_z, off_chunks, total;
+  size_t off_tickets, off_sel, off_counters, off_pp, off_pq, off_z, off_chunks, off_fix, total;
+  size_t zeroed;                 // bytes from the start cleared by every call
 };
 
 // Checks the shape; returns SPECDEC_OK or an error code.
 int check_shape(int B, int gamma, int d, int V, int dtype, int mode) {
   if (dtype != SPECDEC_BF16 && dtype != SPECDEC_FP32) return SPECDEC_ERR_INVALID_ARG;
   if (mode != SPECDEC_SAMPLE && mode != SPECDEC_GREEDY) return SPECDEC_ERR_INVALID_ARG;
-  if (B < 0 || gamma < 1 || gamma > SPECDEC_MAX_GAMMA || d < 1 || V < 1)
+  if (B < 0 || gamma < 1 || gamma > SPECDEC_MAX_GAMMA || d < 1 || V < 1 || V > kMaxVocab)
     return SPECDEC_ERR_UNSUPPORTED;
   if (dtype == SPECDEC_BF16 && d % 8 != 0) return SPECDEC_ERR_UNSUPPORTED;
   const long long M = (long long)B * (gamma + 1);
@@ -37,14 +38,15 @@ int check_shape(int B, int gamma, int d, int V, int dtype, int mode) {
 }
 
 Plan make_plan(int B, int gamma, int d, int V, int dtype, int mode) {
-  (void)d;
-  (void)dtype;
   Plan p;
   p.M = B * (gamma + 1);
-  p.P = (V + kBlockV - 1) / kBlockV;
+  p.P = (V + kBlockV - 1) / kBlockV;   // record capacity per row (>= any grid used)
   p.nchunks = (V + kChunkV - 1) / kChunkV;
   const bool sample = mode == SPECDEC_SAMPLE;
   size_t off = align_up(sizeof(WsHeader));
+  p.off_tickets = off;
+  off = align_up(off + sizeof(int) * (kMaxGrid + 1));
+  p.zeroed = off;
   p.off_sel = off;
   off = align_up(off + sizeof(SelectedRow) * (size_t)B);
   p.off_counters = off;
@@ -57,6 +59,8 @@ Plan make_plan(int B, int gamma, int d, int V, int dtype, int mode) {
   if (sample) off = align_up(off + sizeof(float) * (size_t)p.M * V);
   p.off_chunks = off;
   if (sample) off = align_up(off + sizeof(float) * (size_t)B * p.nchunks);
+  p.off_fix = off;
+  if (dtype == SPECDEC_BF16) off = align_up(off + sizeof(float) * tc_fix_floats(p.M, V, d));
   p.total = off;
   return p;
 }
@@ -102,6 +106,25 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, int rows, int cols, in
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same matrix as a 3-D tensor {64, rows, cols/64} whose slices of 64
+// columns are the outer dimension, with a {64, box_rows, box_slices} box:
+// one load brings box_slices adjacent 128-byte pieces of every row, stored
+// slice-major as box_slices standard [box_rows x 128 B] swizzled tiles.
+// Needs cols % 64 == 0.
+bool encode_bf16_rows3d(CUtensorMap* map, const void* base, int rows, int cols, int box_rows,
+                        int box_slices) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kBlockK, (cuuint64_t)rows,
+                              (cuuint64_t)(cols / kBlockK)};
+  const cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)kBlockK * 2};
+  const cuuint32_t box[3] = {(cuuint32_t)kBlockK, (cuuint32_t)box_rows, (cuuint32_t)box_slices};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Extras {
   float* logits_out = nullptr;
   float* lse_p = nullptr;
@@ -143,8 +166,10 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   float* chunk_sums = reinterpret_cast<float*>(ws + pl.off_chunks);
   const float c = sample ? kLog2e / T : kLog2e;
 
-  // The status word is cleared with the first operation of the call.
-  if (cudaMemsetAsync(status, 0, sizeof(int), stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  // The status word and the fix-up tickets are cleared by the call's first
+  // operation.
+  if (cudaMemsetAsync(status, 0, pl.zeroed, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  int P = pl.P;
 
   EpiParams ep;
   ep.M = pl.M;
@@ -158,14 +183,19 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   ep.dl = draft_logits;
   ep.pp = pp;
   ep.pq = pq;
+  ep.run = nullptr;
+  ep.q_in_epilogue = 1;
 
   if (ex.ev0 && cudaEventRecord(ex.ev0, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
   cudaError_t e;
   if (dtype == SPECDEC_BF16) {
-    const TcGeometry g = tc_geometry(pl.M);
+    const TcGeometry g = tc_geometry(pl.M, V, d, nsm);
     CUtensorMap tw, th;
-    if (!encode_bf16_rows(&tw, W, V, d, kBlockV) || !encode_bf16_rows(&th, hidden, pl.M, d, g.BT))
-      return SPECDEC_ERR_CUDA;
+    const bool ok = g.box3d ? (encode_bf16_rows3d(&tw, W, V, d, kBlockV, g.kc) &&
+                               encode_bf16_rows3d(&th, hidden, pl.M, d, g.BT, g.kc))
+                            : (encode_bf16_rows(&tw, W, V, d, kBlockV) &&
+                               encode_bf16_rows(&th, hidden, pl.M, d, g.BT));
+    if (!ok) return SPECDEC_ERR_CUDA;
     TcLaunch L;
     L.tmap_w = &tw;
     L.tmap_h = &th;
@@ -173,10 +203,11 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
     L.V = V;
     L.d = d;
     L.gamma = gamma;
-    L.BT = g.BT;
-    L.n_tt = g.n_tt;
     L.status = status;
+    L.fix = reinterpret_cast<float*>(ws + pl.off_fix);
+    L.fix_tickets = reinterpret_cast<int*>(ws + pl.off_tickets);
     L.ep = ep;
+    P = g.records;
     e = launch_lmhead_tc(L, nsm, stream);
   } else {
     e = launch_lmhead_f32(static_cast<const float*>(hidden), static_cast<const float*>(W), d, ep,
@@ -189,7 +220,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   A.B = B;
   A.gamma = gamma;
   A.V = V;
-  A.P = pl.P;
+  A.P = P;
   A.mode = mode;
   A.dl_bf16 = dtype == SPECDEC_BF16;
   A.c = c;

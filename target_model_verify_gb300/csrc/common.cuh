@@ -15,6 +15,7 @@ constexpr int kBlockV = 128;        // vocabulary rows per LM-head tile (MMA M)
 constexpr int kBlockK = 64;         // bf16 per 128-byte swizzled smem row
 constexpr int kMaxBT = 256;         // token rows per tile (MMA N) at most
 constexpr int kChunkV = 4096;       // residual-sampler chunk (256 threads x 16)
+constexpr int kMaxVocab = 1 << 22;  // V limit: the sampler stages 1024 chunk sums
 constexpr int kSampleThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -213,6 +214,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// 3-D tiled TMA load of box {x.., y.., z..} into shared memory.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int x,
+                                            int y, int z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
+      : "memory");
+}
+
 // tcgen05 (5th-generation tensor core, accumulators in tensor memory).
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -278,8 +289,141 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// Programmatic dependent launch: wait until the preceding kernel in the
+// stream has completed and its writes are visible (a no-op when this
+// kernel was launched without the programmatic-serialisation attribute).
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Let the next kernel in the stream start launching its CTAs now.
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ------------------------------------- 16-column transposed reductions --
+// Each lane holds one value for each of 16 columns (one vocabulary row of a
+// tile). Five butterfly steps halve the columns a lane carries (16 -> 8 ->
+// 4 -> 2 -> 1) while doubling the lanes folded in, so afterwards lanes 2c
+// and 2c+1 both hold column c reduced over all 32 lanes. The 16 chains are
+// independent, so the shuffles overlap instead of running one column at a
+// time.
+
+// Online-softmax pair merge with one exp2: (ma, sa) <- (ma, sa) + (mb, sb),
+// s = sum of exp2((x - m) * c).
+__device__ __forceinline__ void osm_merge(float& ma, float& sa, float mb, float sb, float c) {
+  const float mm = fmaxf(ma, mb);
+  if (mm == -INFINITY) {
+    ma = mm;
+    sa = 0.f;
+    return;
+  }
+  if (ma >= mb)
+    sa = sa + sb * exp2f((mb - ma) * c);
+  else
+    sa = sb + sa * exp2f((ma - mb) * c);
+  ma = mm;
+}
+
+template <int N>
+__device__ __forceinline__ void osm_halve(float (&m)[16], float (&s)[16], bool upper, int off,
+                                          float c) {
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const float km = upper ? m[N + k] : m[k];
+    const float ks = upper ? s[N + k] : s[k];
+    const float sm = upper ? m[k] : m[N + k];
+    const float ss = upper ? s[k] : s[N + k];
+    const float rm = __shfl_xor_sync(0xffffffffu, sm, off);
+    const float rs = __shfl_xor_sync(0xffffffffu, ss, off);
+    m[k] = km;
+    s[k] = ks;
+    osm_merge(m[k], s[k], rm, rs, c);
+  }
+}
+
+// Per-column (max, sum exp2((x - max) * c)) of x over the warp; -inf values
+// are absent. Result for column (lane >> 1).
+__device__ __forceinline__ void warp_softmax16(const float (&x)[16], float c, float& m_out,
+                                               float& s_out) {
+  const int lane = threadIdx.x & 31;
+  float m[16], s[16];
+  {
+    const bool upper = (lane & 16) != 0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float keep = upper ? x[8 + k] : x[k];
+      const float send = upper ? x[k] : x[8 + k];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+      const float mm = fmaxf(keep, recv);
+      m[k] = mm;
+      s[k] = mm == -INFINITY ? 0.f : 1.f + exp2f(-fabsf(keep - recv) * c);
+    }
+  }
+  osm_halve<4>(m, s, (lane & 8) != 0, 8, c);
+  osm_halve<2>(m, s, (lane & 4) != 0, 4, c);
+  osm_halve<1>(m, s, (lane & 2) != 0, 2, c);
+  const float rm = __shfl_xor_sync(0xffffffffu, m[0], 1);
+  const float rs = __shfl_xor_sync(0xffffffffu, s[0], 1);
+  // The two lanes of a pair merge in the same order, so they agree exactly.
+  float am = m[0], as = s[0];
+  if (lane & 1) {
+    am = rm;
+    as = rs;
+    osm_merge(am, as, m[0], s[0], c);
+  } else {
+    osm_merge(am, as, rm, rs, c);
+  }
+  m_out = am;
+  s_out = as;
+}
+
+template <int N>
+__device__ __forceinline__ void amax_halve(float (&v)[16], int (&i)[16], bool upper, int off) {
+#pragma unroll
+  for (int k = 0; k < N; ++k) {
+    const float kv = upper ? v[N + k] : v[k];
+    const int ki = upper ? i[N + k] : i[k];
+    const float sv = upper ? v[k] : v[N + k];
+    const int si = upper ? i[k] : i[N + k];
+    const float rv = __shfl_xor_sync(0xffffffffu, sv, off);
+    const int ri = __shfl_xor_sync(0xffffffffu, si, off);
+    v[k] = kv;
+    i[k] = ki;
+    if (argmax_better(rv, ri, v[k], i[k])) {
+      v[k] = rv;
+      i[k] = ri;
+    }
+  }
+}
+
+// Per-column (max value, lowest index) over the warp; every value of this
+// lane carries the index `idx`. Result for column (lane >> 1).
+__device__ __forceinline__ void warp_argmax16(const float (&x)[16], int idx, float& v_out,
+                                              int& i_out) {
+  const int lane = threadIdx.x & 31;
+  float v[16];
+  int i[16];
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    v[k] = x[k];
+    i[k] = idx;
+  }
+  amax_halve<8>(v, i, (lane & 16) != 0, 16);
+  amax_halve<4>(v, i, (lane & 8) != 0, 8);
+  amax_halve<2>(v, i, (lane & 4) != 0, 4);
+  amax_halve<1>(v, i, (lane & 2) != 0, 2);
+  const float rv = __shfl_xor_sync(0xffffffffu, v[0], 1);
+  const int ri = __shfl_xor_sync(0xffffffffu, i[0], 1);
+  if (argmax_better(rv, ri, v[0], i[0])) {
+    v[0] = rv;
+    i[0] = ri;
+  }
+  v_out = v[0];
+  i_out = i[0];
 }
 
 // ------------------------------------------------ LM-head tile epilogue --
@@ -287,8 +431,14 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // row of a 128-row tile (4 warps, warp quarter q holds rows 32q..32q+31),
 // each holding the logits of 16 consecutive token rows.
 
+struct RedSlot {
+  float pm, ps, am;
+  int ai;
+  float qm, qs;
+};
+
 struct EpiParams {
-  int M, V, gamma, P;      // P = vocabulary tiles = partial records per row
+  int M, V, gamma, P;      // P = partial records per row
   float c;                 // log2(e) / T
   int sample;              // softmax partials for p and q
   int want_argmax;         // argmax partials
@@ -296,78 +446,89 @@ struct EpiParams {
   const void* dl;          // draft logits [B, gamma, V]
   PartialP* pp;            // [M, P]
   PartialQ* pq;            // [B*gamma, P]
+  RedSlot* run;            // shared memory [M]: fold tiles into one record per
+                           // row and CTA (NULL: one record per row and tile)
+  int q_in_epilogue;       // 1: the epilogue also reduces the draft logits
 };
 
-struct RedSlot {
-  float pm, ps, am;
-  int ai;
-  float qm, qs;
-};
+__device__ __forceinline__ void redslot_merge(RedSlot& a, const RedSlot& o, float c) {
+  softmax_merge(a.pm, a.ps, o.pm, o.ps, c);
+  softmax_merge(a.qm, a.qs, o.qm, o.qs, c);
+  if (argmax_better(o.am, o.ai, a.am, a.ai)) {
+    a.am = o.am;
+    a.ai = o.ai;
+  }
+}
 
+__device__ __forceinline__ RedSlot redslot_empty() {
+  RedSlot r;
+  r.pm = -INFINITY;
+  r.ps = 0.f;
+  r.am = -INFINITY;
+  r.ai = 0x7fffffff;
+  r.qm = -INFINITY;
+  r.qs = 0.f;
+  return r;
+}
+
+// Draft logits of this thread's vocabulary row v for the 16 token rows
+// m0..m0+15 (-inf where the row is not a draft row or v >= V), loaded up
+// front so the 16 loads are in flight together.
 template <typename DL>
-__device__ __forceinline__ void epilogue_chunk16(const float (&acc)[16], int m0, int v, int vt,
-                                                 int q, int lane, int epi_tid, RedSlot* red,
-                                                 const EpiParams& ep, int bar_id) {
+__device__ __forceinline__ void prefetch_draft16(float (&zq)[16], int m0, int v,
+                                                 const EpiParams& ep) {
   const bool vvalid = v < ep.V;
   const int g1 = ep.gamma + 1;
+  const DL* dl = static_cast<const DL*>(ep.dl);
 #pragma unroll
   for (int n = 0; n < 16; ++n) {
     const int m = m0 + n;
-    if (m >= ep.M) break;
-    const float z = acc[n];
-    if (ep.zout != nullptr && vvalid) __stcs(ep.zout + (size_t)m * ep.V + v, z);
-    RedSlot r;
-    r.pm = -INFINITY;
-    r.ps = 0.f;
-    r.qm = -INFINITY;
-    r.qs = 0.f;
-    r.am = -INFINITY;
-    r.ai = 0x7fffffff;
-    if (ep.sample) {
-      const float zm = vvalid ? z : -INFINITY;
-      const float mx = warp_max(zm);
-      const float e = vvalid ? exp2f((z - mx) * ep.c) : 0.f;
-      r.pm = mx;
-      r.ps = warp_sum(e);
-      const int b = m / g1;
-      const int i = m - b * g1;
-      if (i < ep.gamma) {
-        const DL* dl = static_cast<const DL*>(ep.dl);
-        const float zq = vvalid ? load_logit(dl, ((size_t)b * ep.gamma + i) * ep.V + v) : -INFINITY;
-        const float mq = warp_max(zq);
-        const float eq = vvalid ? exp2f((zq - mq) * ep.c) : 0.f;
-        r.qm = mq;
-        r.qs = warp_sum(eq);
-      }
-    }
-    if (ep.want_argmax) {
-      float av = vvalid ? z : -INFINITY;
-      int ai = vvalid ? v : 0x7fffffff;
-      warp_argmax(av, ai);
-      r.am = av;
-      r.ai = ai;
-    }
-    if (lane == 0) red[q * 16 + n] = r;
+    const int b = m / g1;
+    const int i = m - b * g1;
+    zq[n] = (ep.sample && vvalid && m < ep.M && i < ep.gamma)
+                ? load_logit(dl, ((size_t)b * ep.gamma + i) * ep.V + v)
+                : -INFINITY;
   }
+}
+
+template <typename DL>
+__device__ __forceinline__ void epilogue_chunk16(const float (&acc)[16], const float (&zqv)[16],
+                                                 int m0, int v, int vt, int q, int lane,
+                                                 int epi_tid, RedSlot* red, const EpiParams& ep,
+                                                 int bar_id) {
+  const bool vvalid = v < ep.V;
+  const int g1 = ep.gamma + 1;
+  if (ep.zout != nullptr && vvalid) {
+#pragma unroll
+    for (int n = 0; n < 16; ++n)
+      if (m0 + n < ep.M) __stcs(ep.zout + (size_t)(m0 + n) * ep.V + v, acc[n]);
+  }
+  RedSlot r = redslot_empty();
+  float zm[16];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) zm[n] = vvalid ? acc[n] : -INFINITY;
+  if (ep.sample) {
+    warp_softmax16(zm, ep.c, r.pm, r.ps);
+    if (ep.q_in_epilogue) warp_softmax16(zqv, ep.c, r.qm, r.qs);
+  }
+  if (ep.want_argmax) warp_argmax16(zm, vvalid ? v : 0x7fffffff, r.am, r.ai);
+  if ((lane & 1) == 0) red[q * 16 + (lane >> 1)] = r;
   named_bar_sync(bar_id, 128);
   if (epi_tid < 16) {
     const int m = m0 + epi_tid;
     if (m < ep.M) {
       RedSlot a = red[epi_tid];
 #pragma unroll
-      for (int qq = 1; qq < 4; ++qq) {
-        const RedSlot o = red[qq * 16 + epi_tid];
-        softmax_merge(a.pm, a.ps, o.pm, o.ps, ep.c);
-        softmax_merge(a.qm, a.qs, o.qm, o.qs, ep.c);
-        if (argmax_better(o.am, o.ai, a.am, a.ai)) {
-          a.am = o.am;
-          a.ai = o.ai;
-        }
+      for (int qq = 1; qq < 4; ++qq) redslot_merge(a, red[qq * 16 + epi_tid], ep.c);
+      if (ep.run != nullptr) {
+        redslot_merge(ep.run[m], a, ep.c);   // this thread owns row m's slot
+      } else {
+        ep.pp[(size_t)m * ep.P + vt] = PartialP{a.pm, a.ps, a.am, a.ai};
+        const int b = m / g1;
+        const int i = m - b * g1;
+        if (ep.sample && ep.q_in_epilogue && i < ep.gamma)
+          ep.pq[((size_t)b * ep.gamma + i) * ep.P + vt] = PartialQ{a.qm, a.qs};
       }
-      ep.pp[(size_t)m * ep.P + vt] = PartialP{a.pm, a.ps, a.am, a.ai};
-      const int b = m / g1;
-      const int i = m - b * g1;
-      if (ep.sample && i < ep.gamma) ep.pq[((size_t)b * ep.gamma + i) * ep.P + vt] = PartialQ{a.qm, a.qs};
     }
   }
   named_bar_sync(bar_id, 128);

@@ -16,9 +16,9 @@ struct TcLaunch {
   const CUtensorMap* tmap_w;     // W_lm [V, d], box {64, 128}, 128B swizzle
   const CUtensorMap* tmap_h;     // hidden [M, d], box {64, BT}, 128B swizzle
   int M, V, d, gamma;
-  int BT;                        // token rows per tile: multiple of 16, <= 256
-  int n_tt;                      // token tiles
   int* status;
+  float* fix;                    // stream-K fix-up slots (tc_fix_floats floats)
+  int* fix_tickets;              // kMaxGrid + 1 ints, zero at launch
   EpiParams ep;
 };
 cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream);
@@ -67,10 +67,24 @@ cudaError_t launch_sample(const SampleLaunch& L, cudaStream_t stream);
 cudaError_t launch_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose, float* out,
                                    cudaStream_t stream);
 
-// Tile geometry of the tensor-core path, shared by the planner and launcher.
+// Tile geometry and schedule of the tensor-core path, shared by the
+// workspace planner and the launcher.
+constexpr int kMaxGrid = 256;    // persistent CTAs at most (one per SM)
 struct TcGeometry {
-  int BT, n_tt, stages, stage_bytes, tmem_cols, smem_bytes;
+  int BT;                        // token rows per tile: multiple of 16, <= 256
+  int n_tt;                      // token tiles
+  int kc;                        // 64-wide k slices per shared-memory stage
+  int box3d;                     // 3-D boxes {64, rows, kc} (d % 64 == 0)
+  int stages, stage_bytes, tmem_cols, smem_bytes;
+  int n_units, nk, grid;
+  int stream_k;                  // one token tile: contiguous k-iteration ranges
+  int records;                   // partial records per row (grid or vocabulary tiles)
 };
-TcGeometry tc_geometry(int M);
+TcGeometry tc_geometry(int M, int V, int d, int num_sms);
+// Floats of stream-K fix-up storage for a shape (0 without stream-K).
+inline size_t tc_fix_floats(int M, int V, int d) {
+  const TcGeometry g = tc_geometry(M, V, d, kMaxGrid);
+  return g.stream_k ? (size_t)(kMaxGrid + 1) * 2 * g.BT * kBlockV : 0;
+}
 
 }  // namespace specdec

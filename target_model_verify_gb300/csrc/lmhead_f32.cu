@@ -47,7 +47,9 @@ __global__ void __launch_bounds__(128)
     }
     __syncthreads();
   }
-  epilogue_chunk16<float>(acc, m0, v, vt, tid >> 5, tid & 31, tid, red, ep, 1);
+  float zq[16];
+  prefetch_draft16<float>(zq, m0, v, ep);
+  epilogue_chunk16<float>(acc, zq, m0, v, vt, tid >> 5, tid & 31, tid, red, ep, 1);
 }
 
 }  // namespace

@@ -8,19 +8,37 @@
 //
 // Layout: swap-AB. The MMA's M dimension is a 128-row tile of W_lm (the
 // vocabulary), its N dimension the BT token rows, so z^T[v, m] lands in
-// tensor memory with one vocabulary row per TMEM lane. Work units are
-// (vocabulary tile, token tile) pairs, token tile fastest, dealt round-robin
-// to one persistent CTA per SM; CTAs that run together share the W tile in
-// L2 when there is more than one token tile.
+// tensor memory with one vocabulary row per TMEM lane. A work unit is a
+// (vocabulary tile, token tile) pair; its k dimension is nk k-steps, each
+// one shared-memory stage of C adjacent slices of 64 (C = 4 at small batch).
+// With d % 64 == 0 the loads are 3-D boxes {64, rows, C}, so each W row
+// contributes C*128 contiguous bytes per request: fewer, longer DRAM bursts,
+// which measured ~7.1 TB/s against ~6.8 TB/s for one 128-byte slice per row.
 //
-// Warp roles (192 threads):
+// Scheduling, one persistent CTA per SM:
+//   * one token tile (M <= 256, every small-batch shape): stream-K. The
+//     n_units * nk (unit, k-step) iterations are cut into equal contiguous
+//     ranges, one per CTA, so every SM streams the same number of W bytes.
+//     A unit cut between two CTAs leaves each a partial accumulator; both
+//     write theirs to a fix-up slot and take an atomic ticket, and the
+//     second to arrive adds the two and runs the epilogue (nobody waits).
+//     Each CTA folds the softmax partials of all its tiles into one record
+//     per token row.
+//   * several token tiles: units dealt round-robin with the token tile
+//     fastest, so the CTAs that share a W tile run together and read it
+//     once from HBM and the rest from L2; one record per (row, tile).
+//
+// Warp roles (320 threads):
 //   warp 0     one thread issues TMA loads of W and hidden k-slices into a
 //              ring of shared-memory stages (full/empty mbarriers).
 //   warp 1     allocates tensor memory; one thread issues tcgen05.mma into
 //              one of two TMEM accumulators and commits to mbarriers.
 //   warps 2-5  epilogue: tcgen05.ld of the accumulator, fp32 logits out,
-//              per-tile softmax / argmax partials for p, and the matching
-//              partials of the draft logits for q.
+//              softmax / argmax partials for p.
+//   warps 6-9  q-warps: stream the draft logits of the same vocabulary tiles
+//              (8 rows in flight per warp) and reduce their softmax
+//              partials for q, off the epilogue's critical path. The CTA
+//              holding a unit's first k-step scores that unit's draft rows.
 // Every wait is bounded (1 s); a timeout records SPECDEC_ERR_TIMEOUT, stops
 // the other roles, waits for copies and MMAs already issued, frees tensor
 // memory and returns.
@@ -31,19 +49,67 @@
 namespace specdec {
 namespace {
 
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kQRowsInFlight = 8;
 constexpr int kStageA = kBlockV * kBlockK * 2;   // 16 KB of W per stage
-constexpr int kMaxStages = 12;
+constexpr int kMaxStagesC1 = 10;   // stage caps by slices per stage (measured)
+constexpr int kMaxStagesC2 = 4;
+constexpr int kMaxStagesC4 = 3;
 constexpr int kSmemLimit = 232448;               // 227 KB opt-in per CTA
-constexpr int kMiscBytes = 4096;
+constexpr int kMiscBytes = 2048;   // mbarriers, flags and the 64 cross-warp slots
 constexpr unsigned long long kDrainLimitNs = 100000000ull;
+constexpr int kRunBytes = kMaxBT * (int)(sizeof(RedSlot) + sizeof(PartialQ));
+constexpr int kMaxDevices = 64;
 
 struct TcParams {
   int M, V, d, gamma;
   int BT, n_tt, n_units, nk, stages;
+  int kc;                        // 64-wide k slices per stage (C)
+  int box3d;                     // 1: 3-D boxes {64, rows, C}; 0: 2-D boxes, C = 1
+  int stream_k;                  // 1: contiguous iteration ranges (one token tile)
+  long long total_iters;         // n_units * nk (k-steps)
   uint32_t stage_bytes, tmem_cols;
   int* status;
+  float* fix;                    // [(grid+1) * 2][BT * 128] partial accumulators
+  int* fix_tickets;              // [grid+1], zero at launch
   EpiParams ep;
+};
+
+// One stretch of work: k-steps [kb, ke) of unit `unit`.
+struct Piece {
+  int unit, kb, ke;
+};
+
+// The sequence of pieces a CTA processes; all three roles walk it alike.
+struct PieceIter {
+  long long it, end;
+  int unit;
+  __device__ PieceIter(const TcParams& p) {
+    if (p.stream_k) {
+      it = p.total_iters * blockIdx.x / gridDim.x;
+      end = p.total_iters * (blockIdx.x + 1) / gridDim.x;
+    } else {
+      unit = blockIdx.x;
+    }
+  }
+  __device__ bool next(const TcParams& p, Piece& pc) {
+    if (p.stream_k) {
+      if (it >= end) return false;
+      const long long u = it / p.nk;
+      pc.unit = (int)u;
+      pc.kb = (int)(it - u * p.nk);
+      const long long rem = end - it;
+      pc.ke = (int)((long long)pc.kb + rem < (long long)p.nk ? pc.kb + rem : p.nk);
+      it += pc.ke - pc.kb;
+      return true;
+    }
+    if (unit >= p.n_units) return false;
+    pc.unit = unit;
+    pc.kb = 0;
+    pc.ke = p.nk;
+    unit += gridDim.x;
+    return true;
+  }
 };
 
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
@@ -76,8 +142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t mma_done_bar = bar0 + 8u * (2 * S + 4);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  volatile int* epi_ok = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* epi_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
   RedSlot* red = reinterpret_cast<RedSlot*>(misc + 8 * (2 * S + 5) + 64);
+  RedSlot* run = red + 64;       // [BT] per-row records folded over the CTA's tiles
+  PartialQ* qrun = reinterpret_cast<PartialQ*>(run + kMaxBT);   // [BT] draft rows, likewise
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -95,6 +163,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_mbar_init();
   }
+  if (p.stream_k)
+    for (int r = threadIdx.x; r < p.BT; r += kThreads) {
+      run[r] = redslot_empty();
+      qrun[r] = PartialQ{-INFINITY, 0.f};
+    }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
   tc_fence_before();
   __syncthreads();
@@ -110,18 +183,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       uint32_t issued_mask = 0, issued_phase = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < p.n_units; unit += gridDim.x) {
-        const int vt = unit / p.n_tt;
-        const int tt = unit - vt * p.n_tt;
-        for (int kc = 0; kc < p.nk; ++kc) {
+      PieceIter itr(p);
+      Piece pc;
+      while (ok && itr.next(p, pc)) {
+        const int vt = pc.unit / p.n_tt;
+        const int tt = pc.unit - vt * p.n_tt;
+        for (int kc = pc.kb; kc < pc.ke; ++kc) {
           if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(full_bar(s), p.stage_bytes);
           const uint32_t a = sbase + (uint32_t)s * p.stage_bytes;
-          tma_load_2d(a, &tmap_w, full_bar(s), kc * kBlockK, vt * kBlockV, pol_w);
-          tma_load_2d(a + kStageA, &tmap_h, full_bar(s), kc * kBlockK, tt * p.BT, pol_h);
+          const uint32_t h = a + (uint32_t)(p.kc * kStageA);
+          if (p.box3d) {
+            tma_load_3d(a, &tmap_w, full_bar(s), 0, vt * kBlockV, kc * p.kc, pol_w);
+            tma_load_3d(h, &tmap_h, full_bar(s), 0, tt * p.BT, kc * p.kc, pol_h);
+          } else {
+            tma_load_2d(a, &tmap_w, full_bar(s), kc * kBlockK, vt * kBlockV, pol_w);
+            tma_load_2d(h, &tmap_h, full_bar(s), kc * kBlockK, tt * p.BT, pol_h);
+          }
           issued_mask |= 1u << s;
           issued_phase = (issued_phase & ~(1u << s)) | (ph << s);
           if (++s == S) {
@@ -144,7 +225,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t ph = 0;
       int ul = 0;
       bool ok = true;
-      for (int unit = blockIdx.x; ok && unit < p.n_units; unit += gridDim.x, ++ul) {
+      PieceIter itr(p);
+      Piece pc;
+      while (ok && itr.next(p, pc)) {
         const int acc = ul & 1;
         const uint32_t aph = (uint32_t)(ul >> 1) & 1u;
         if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) {
@@ -153,18 +236,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.BT);
-        for (int kc = 0; kc < p.nk; ++kc) {
+        for (int kc = pc.kb; kc < pc.ke; ++kc) {
           if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a = sbase + (uint32_t)s * p.stage_bytes;
-          const uint64_t adesc = smem_desc_sw128(a);
-          const uint64_t bdesc = smem_desc_sw128(a + kStageA);
+          const uint32_t h = a + (uint32_t)(p.kc * kStageA);
+          for (int c = 0; c < p.kc; ++c) {
+            // slice c: W rows [128 x 128 B] at a + c*16 KB, hidden [BT x 128 B]
+            const uint64_t adesc = smem_desc_sw128(a + (uint32_t)(c * kStageA));
+            const uint64_t bdesc = smem_desc_sw128(h + (uint32_t)(c * p.BT * kBlockK * 2));
 #pragma unroll
-          for (int k = 0; k < kBlockK / 16; ++k)
-            tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, (kc | k) ? 1u : 0u);
+            for (int k = 0; k < kBlockK / 16; ++k)
+              tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
+                          (kc > pc.kb || c > 0 || k > 0) ? 1u : 0u);
+          }
           tc_commit(empty_bar(s));
           if (++s == S) {
             s = 0;
@@ -173,39 +261,155 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (!ok) break;
         tc_commit(tfull_bar(acc));
+        ++ul;
       }
       // All MMAs this thread issued are complete once this phase ends.
       tc_commit(mma_done_bar);
       mbar_wait_drain(mma_done_bar, 0);
     }
+  } else if (warp >= 6) {
+    // ---------------------------------------------------------- q-warps --
+    if (p.ep.sample) {
+      const int qw = warp - 6;
+      const int g1 = p.gamma + 1;
+      const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(p.ep.dl);
+      PieceIter itr(p);
+      Piece pc;
+      while (itr.next(p, pc)) {
+        if (pc.kb != 0) continue;
+        const int vt = pc.unit / p.n_tt;
+        const int tt = pc.unit - vt * p.n_tt;
+        const int m_lo = tt * p.BT;
+        const int m_hi = min(p.M, m_lo + p.BT);
+        // Draft rows of token rows [m_lo, m_hi): a contiguous range.
+        const int dr_lo = (m_lo / g1) * p.gamma + min(m_lo % g1, p.gamma);
+        const int dr_hi = (m_hi / g1) * p.gamma + min(m_hi % g1, p.gamma);
+        const int v0 = vt * kBlockV;
+        for (int r0 = dr_lo + qw; r0 < dr_hi; r0 += 4 * kQRowsInFlight) {
+          float x[kQRowsInFlight][4];
+#pragma unroll
+          for (int g = 0; g < kQRowsInFlight; ++g) {
+            const int r = r0 + 4 * g;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int v = v0 + lane + 32 * e;
+              x[g][e] = (r < dr_hi && v < p.V) ? __bfloat162float(dl[(size_t)r * p.V + v])
+                                                : -INFINITY;
+            }
+          }
+#pragma unroll
+          for (int g = 0; g < kQRowsInFlight; ++g) {
+            const int r = r0 + 4 * g;
+            float m = fmaxf(fmaxf(x[g][0], x[g][1]), fmaxf(x[g][2], x[g][3]));
+            float sum = 0.f;
+            if (m != -INFINITY) {
+#pragma unroll
+              for (int e = 0; e < 4; ++e) sum += exp2f((x[g][e] - m) * p.ep.c);
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+              const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+              const float s2 = __shfl_xor_sync(0xffffffffu, sum, o);
+              osm_merge(m, sum, m2, s2, p.ep.c);
+            }
+            if (lane == 0 && r < dr_hi) {
+              if (p.stream_k) {
+                osm_merge(qrun[r].m, qrun[r].s, m, sum, p.ep.c);   // warp r % 4 owns slot r
+              } else {
+                p.ep.pq[(size_t)r * p.ep.P + vt] = PartialQ{m, sum};
+              }
+            }
+          }
+        }
+      }
+      if (p.stream_k) {
+        named_bar_sync(3, 128);
+        const int n_draft = (p.M / g1) * p.gamma + min(p.M % g1, p.gamma);
+        for (int r = threadIdx.x - 192; r < n_draft; r += 128)
+          p.ep.pq[(size_t)r * p.ep.P + blockIdx.x] = qrun[r];
+      }
+    }
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int epi_tid = threadIdx.x - 64;
+    const int row = q * 32 + lane;          // vocabulary row within the tile
+    EpiParams ep = p.ep;
+    ep.run = p.stream_k ? run : nullptr;
+    const size_t slot_floats = (size_t)p.BT * kBlockV;
     int ul = 0;
-    for (int unit = blockIdx.x; unit < p.n_units; unit += gridDim.x, ++ul) {
+    PieceIter itr(p);
+    Piece pc;
+    while (itr.next(p, pc)) {
       const int acc = ul & 1;
       const uint32_t aph = (uint32_t)(ul >> 1) & 1u;
-      if (epi_tid == 0) *epi_ok = mbar_wait(tfull_bar(acc), aph, abort_flag, p.status) ? 1 : 0;
+      ++ul;
+      const int vt = pc.unit / p.n_tt;
+      const int tt = pc.unit - vt * p.n_tt;
+      const int v = vt * kBlockV + row;
+      const int m_base = tt * p.BT;
+      if (epi_tid == 0) *epi_flag = mbar_wait(tfull_bar(acc), aph, abort_flag, p.status) ? 1 : 0;
       named_bar_sync(1, 128);
-      const bool ok = *epi_ok != 0;
+      const bool ok = *epi_flag != 0;
       named_bar_sync(2, 128);
       if (!ok) break;
       tc_fence_after();
-      const int vt = unit / p.n_tt;
-      const int tt = unit - vt * p.n_tt;
-      const int v = vt * kBlockV + q * 32 + lane;
-      const int m_base = tt * p.BT;
+      const int n_chunks = (min(p.BT, p.M - m_base) + 15) / 16;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.BT);
-      for (int c = 0; c < p.BT / 16; ++c) {
-        const int m0 = m_base + c * 16;
-        if (m0 >= p.M) break;
-        float accv[16];
-        tmem_ld16(tbase + (uint32_t)(c * 16), accv);
-        epilogue_chunk16<DL>(accv, m0, v, vt, q, lane, epi_tid, red, p.ep, 1);
+
+      bool finish = true;
+      const float* other = nullptr;
+      if (pc.kb > 0 || pc.ke < p.nk) {
+        // A unit shared with a neighbouring CTA: the piece holding k-slice 0
+        // is part A of the boundary slot after its CTA, the other part B.
+        const int slot = pc.kb > 0 ? (int)blockIdx.x : (int)blockIdx.x + 1;
+        const int part = pc.kb > 0 ? 1 : 0;
+        float* mine = p.fix + ((size_t)slot * 2 + part) * slot_floats;
+        other = p.fix + ((size_t)slot * 2 + (1 - part)) * slot_floats;
+        for (int c = 0; c < n_chunks; ++c) {
+          float accv[16];
+          tmem_ld16(tbase + (uint32_t)(c * 16), accv);
+#pragma unroll
+          for (int n = 0; n < 16; ++n) __stcg(mine + (size_t)(c * 16 + n) * kBlockV + row, accv[n]);
+        }
+        __threadfence();
+        named_bar_sync(1, 128);
+        if (epi_tid == 0) {
+          const int ticket = atomicAdd(p.fix_tickets + slot, 1);
+          __threadfence();
+          *epi_flag = ticket == 1 ? 1 : 0;
+        }
+        named_bar_sync(1, 128);
+        finish = *epi_flag != 0;
+        named_bar_sync(2, 128);
+        if (finish) __threadfence();
+      }
+      if (finish) {
+        float zq[16];   // draft logits are reduced by the q-warps
+#pragma unroll
+        for (int n = 0; n < 16; ++n) zq[n] = -INFINITY;
+        for (int c = 0; c < n_chunks; ++c) {
+          float accv[16];
+          tmem_ld16(tbase + (uint32_t)(c * 16), accv);
+          if (other != nullptr) {
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+              accv[n] += __ldcg(other + (size_t)(c * 16 + n) * kBlockV + row);
+          }
+          epilogue_chunk16<DL>(accv, zq, m_base + c * 16, v, vt, q, lane, epi_tid, red, ep, 1);
+        }
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
+    }
+    if (p.stream_k) {
+      // One record per token row for everything this CTA finished.
+      named_bar_sync(1, 128);
+      const int g1 = p.gamma + 1;
+      for (int m = epi_tid; m < p.M; m += 128) {
+        const RedSlot a = run[m];
+        p.ep.pp[(size_t)m * p.ep.P + blockIdx.x] = PartialP{a.pm, a.ps, a.am, a.ai};
+      }
     }
   }
 
@@ -217,9 +421,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <typename DL>
-cudaError_t launch_typed(const TcLaunch& L, int num_sms, cudaStream_t stream) {
-  const TcGeometry g = tc_geometry(L.M);
+}  // namespace
+
+TcGeometry tc_geometry(int M, int V, int d, int num_sms) {
+  TcGeometry g;
+  g.n_tt = (M + kMaxBT - 1) / kMaxBT;
+  if (g.n_tt < 1) g.n_tt = 1;
+  const int per = (M + g.n_tt - 1) / g.n_tt;
+  g.BT = ((per + 15) / 16) * 16;
+  if (g.BT < 16) g.BT = 16;
+  // Slices per stage: 4 while three such stages fit, else 2 while four fit,
+  // else 1 (the stream rates these caps were chosen from are in the kernel
+  // header comment).
+  const int budget = kSmemLimit - 1024 - kMiscBytes - kRunBytes;
+  const int slice_bytes = kStageA + g.BT * kBlockK * 2;
+  g.box3d = d % kBlockK == 0 ? 1 : 0;
+  if (g.box3d && budget / (4 * slice_bytes) >= 3) {
+    g.kc = 4;
+  } else if (g.box3d && budget / (2 * slice_bytes) >= 4) {
+    g.kc = 2;
+  } else {
+    g.kc = 1;
+  }
+  g.stage_bytes = g.kc * slice_bytes;
+  const int cap = g.kc == 4 ? kMaxStagesC4 : g.kc == 2 ? kMaxStagesC2 : kMaxStagesC1;
+  int stages = budget / g.stage_bytes;
+  if (stages > cap) stages = cap;
+  g.stages = stages;
+  int cols = 32;
+  while (cols < 2 * g.BT) cols <<= 1;
+  g.tmem_cols = cols;
+  g.smem_bytes = 1024 + g.stages * g.stage_bytes + kMiscBytes + kRunBytes;
+  const int n_vt = (V + kBlockV - 1) / kBlockV;
+  g.n_units = n_vt * g.n_tt;
+  g.nk = ((d + kBlockK - 1) / kBlockK + g.kc - 1) / g.kc;
+  int sms = num_sms < kMaxGrid ? num_sms : kMaxGrid;
+  g.grid = g.n_units < sms ? g.n_units : sms;
+  g.stream_k = g.n_tt == 1 ? 1 : 0;
+  g.records = g.stream_k ? g.grid : n_vt;
+  return g;
+}
+
+cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream) {
+  const TcGeometry g = tc_geometry(L.M, L.V, L.d, num_sms);
   TcParams p;
   p.M = L.M;
   p.V = L.V;
@@ -227,46 +471,36 @@ cudaError_t launch_typed(const TcLaunch& L, int num_sms, cudaStream_t stream) {
   p.gamma = L.gamma;
   p.BT = g.BT;
   p.n_tt = g.n_tt;
-  const int n_vt = (L.V + kBlockV - 1) / kBlockV;
-  p.n_units = n_vt * g.n_tt;
-  p.nk = (L.d + kBlockK - 1) / kBlockK;
+  p.n_units = g.n_units;
+  p.nk = g.nk;
+  p.kc = g.kc;
+  p.box3d = g.box3d;
   p.stages = g.stages;
+  p.stream_k = g.stream_k;
+  p.total_iters = (long long)g.n_units * g.nk;
   p.stage_bytes = (uint32_t)g.stage_bytes;
   p.tmem_cols = (uint32_t)g.tmem_cols;
   p.status = L.status;
+  p.fix = L.fix;
+  p.fix_tickets = L.fix_tickets;
   p.ep = L.ep;
-  auto kern = lmhead_tc_kernel<DL>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       g.smem_bytes);
-  if (e != cudaSuccess) return e;
-  const int grid = p.n_units < num_sms ? p.n_units : num_sms;
-  kern<<<grid, kThreads, g.smem_bytes, stream>>>(*L.tmap_w, *L.tmap_h, p);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-TcGeometry tc_geometry(int M) {
-  TcGeometry g;
-  g.n_tt = (M + kMaxBT - 1) / kMaxBT;
-  if (g.n_tt < 1) g.n_tt = 1;
-  const int per = (M + g.n_tt - 1) / g.n_tt;
-  g.BT = ((per + 15) / 16) * 16;
-  if (g.BT < 16) g.BT = 16;
-  g.stage_bytes = kStageA + g.BT * kBlockK * 2;
-  int stages = (kSmemLimit - 1024 - kMiscBytes) / g.stage_bytes;
-  if (stages > kMaxStages) stages = kMaxStages;
-  g.stages = stages;
-  int cols = 32;
-  while (cols < 2 * g.BT) cols <<= 1;
-  g.tmem_cols = cols;
-  g.smem_bytes = 1024 + g.stages * g.stage_bytes + kMiscBytes;
-  return g;
-}
-
-cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream) {
+  p.ep.P = g.records;
+  p.ep.run = nullptr;
+  p.ep.q_in_epilogue = 0;
   // The tensor-core path exists for bf16 inputs; draft logits share the dtype.
-  return launch_typed<__nv_bfloat16>(L, num_sms, stream);
+  auto kern = lmhead_tc_kernel<__nv_bfloat16>;
+  // The shared-memory opt-in is set once per device and size.
+  static int smem_set[kMaxDevices] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices || smem_set[dev] != g.smem_bytes) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices) smem_set[dev] = g.smem_bytes;
+  }
+  kern<<<g.grid, kThreads, g.smem_bytes, stream>>>(*L.tmap_w, *L.tmap_h, p);
+  return cudaGetLastError();
 }
 
 }  // namespace specdec

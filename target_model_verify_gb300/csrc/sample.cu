@@ -17,6 +17,7 @@ namespace specdec {
 namespace {
 
 constexpr int kPer = kChunkV / kSampleThreads;   // 16 tokens per thread
+constexpr int kMaxChunks = kMaxVocab / kChunkV;
 
 template <typename DL>
 __device__ __forceinline__ void chunk_weights(const float* __restrict__ zr,
@@ -57,6 +58,7 @@ template <typename DL>
 __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaunch L) {
   __shared__ float red[kSampleThreads / 32];
   __shared__ float wscan[kSampleThreads / 32];
+  __shared__ float s_cs[kMaxChunks];
   __shared__ int s_last;
   __shared__ int s_tok;
   __shared__ int s_lastpos;
@@ -66,6 +68,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
 
   const int b = blockIdx.y;
   const int chunk = blockIdx.x;
+  grid_dependency_wait();      // the acceptance kernel's selection is complete
   const SelectedRow sr = L.sel[b];
   if (sr.j < 0) return;
   const int g1 = L.gamma + 1;
@@ -92,10 +95,12 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
 
   // ---- last CTA of sequence b: locate the chunk holding t = u * S ----
   const float u = sample_uniform(L.seed, b, sr.j);
+  for (int k = tid; k < L.nchunks; k += kSampleThreads)
+    s_cs[k] = __ldcg(L.chunk_sums + (size_t)b * L.nchunks + k);
+  __syncthreads();
   if (tid == 0) {
-    const volatile float* cs = L.chunk_sums + (size_t)b * L.nchunks;
     float S = 0.f;
-    for (int k = 0; k < L.nchunks; ++k) S += cs[k];
+    for (int k = 0; k < L.nchunks; ++k) S += s_cs[k];
     s_residual = sr.residual;
     if (sr.residual && !(S > 0.f)) s_residual = 0;   // p == q to rounding: draw from p
     s_t = u * S;
@@ -110,19 +115,18 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
 #pragma unroll
       for (int e = 0; e < kPer; ++e) t2 += wk[e];
       const float tot = block_sum(t2, red);
-      if (tid == 0) L.chunk_sums[(size_t)b * L.nchunks + k] = tot;
+      if (tid == 0) s_cs[k] = tot;
     }
     __syncthreads();
     if (tid == 0) {
-      const volatile float* cs = L.chunk_sums + (size_t)b * L.nchunks;
       float S = 0.f;
-      for (int k = 0; k < L.nchunks; ++k) S += cs[k];
+      for (int k = 0; k < L.nchunks; ++k) S += s_cs[k];
       s_t = u * S;
     }
     __syncthreads();
   }
   if (tid == 0) {
-    const volatile float* cs = L.chunk_sums + (size_t)b * L.nchunks;
+    const float* cs = s_cs;
     const float t = s_t;
     float acc = 0.f;
     int found = -1, last_pos = 0;
@@ -188,12 +192,17 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
 }  // namespace
 
 cudaError_t launch_sample(const SampleLaunch& L, cudaStream_t stream) {
-  const dim3 grid(L.nchunks, L.B);
-  if (L.dl_bf16)
-    sample_kernel<__nv_bfloat16><<<grid, kSampleThreads, 0, stream>>>(L);
-  else
-    sample_kernel<float><<<grid, kSampleThreads, 0, stream>>>(L);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.nchunks, L.B);
+  cfg.blockDim = dim3(kSampleThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (L.dl_bf16) return cudaLaunchKernelEx(&cfg, sample_kernel<__nv_bfloat16>, L);
+  return cudaLaunchKernelEx(&cfg, sample_kernel<float>, L);
 }
 
 }  // namespace specdec

@@ -180,6 +180,19 @@ def time_oracle(w, inp, mode, budget_s: float, min_steps: int = 1):
     return n / (time.perf_counter() - t0), n
 
 
+# Draft rows up to which the LM-head kernel reduces q itself; beyond, the
+# library runs its standalone q-statistics kernel first (kQWarpMaxRows).
+Q_WARP_MAX_ROWS = 16
+
+
+def kernels_per_step(w, mode) -> int:
+    """Library kernels one step launches: LM head, accept, (sample), (q stats)."""
+    if mode != wl.SAMPLE:
+        return 2
+    q_stream = w.dtype == "bf16" and w.B * w.gamma > Q_WARP_MAX_ROWS
+    return 3 + (1 if q_stream else 0)
+
+
 # ------------------------------------------------------------ our arm --
 
 def run_ours(args, world, rank, local):
@@ -313,7 +326,7 @@ def run_ours(args, world, rank, local):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,
-        "gpu_launches": K * (3 if mode == wl.SAMPLE else 2),
+        "gpu_launches": K * kernels_per_step(w, mode),
         "clocks": clocks,
     }
     print(json.dumps(line), flush=True)

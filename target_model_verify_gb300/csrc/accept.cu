@@ -73,13 +73,13 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
       }
     } else {
       const int i = r - g1;
-      const PartialQ* row = a.pq + ((size_t)b * gamma + i) * a.P;
-      for (int base = lane; base < a.P; base += 32 * kBatch) {
+      const PartialQ* row = a.pq + ((size_t)b * gamma + i) * a.Pq;
+      for (int base = lane; base < a.Pq; base += 32 * kBatch) {
         PartialQ x[kBatch];
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) {
           const int t = base + 32 * u;
-          x[u] = t < a.P ? row[t] : PartialQ{-INFINITY, 0.f};
+          x[u] = t < a.Pq ? row[t] : PartialQ{-INFINITY, 0.f};
         }
 #pragma unroll
         for (int u = 0; u < kBatch; ++u) softmax_merge(m, s, x[u].m, x[u].s, a.c);

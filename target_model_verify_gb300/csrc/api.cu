@@ -40,12 +40,12 @@ int check_shape(int B, int gamma, int d, int V, int dtype, int mode) {
 Plan make_plan(int B, int gamma, int d, int V, int dtype, int mode) {
   Plan p;
   p.M = B * (gamma + 1);
-  p.P = (V + kBlockV - 1) / kBlockV;   // record capacity per row (>= any grid used)
+  p.P = (V + kBlockV - 1) / kBlockV + 2;   // record capacity per row (>= any grid used)
   p.nchunks = (V + kChunkV - 1) / kChunkV;
   const bool sample = mode == SPECDEC_SAMPLE;
   size_t off = align_up(sizeof(WsHeader));
   p.off_tickets = off;
-  off = align_up(off + sizeof(int) * (kMaxGrid + 1));
+  off = align_up(off + sizeof(int) * kFixSlots);
   p.zeroed = off;
   p.off_sel = off;
   off = align_up(off + sizeof(SelectedRow) * (size_t)B);
@@ -169,13 +169,13 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   // The status word and the fix-up tickets are cleared by the call's first
   // operation.
   if (cudaMemsetAsync(status, 0, pl.zeroed, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
-  int P = pl.P;
+  int P = (V + kBlockV - 1) / kBlockV;   // records per row written by the fp32 kernel
 
   EpiParams ep;
   ep.M = pl.M;
   ep.V = V;
   ep.gamma = gamma;
-  ep.P = pl.P;
+  ep.P = P;
   ep.c = c;
   ep.sample = sample ? 1 : 0;
   ep.want_argmax = (!sample || ex.argmax_out) ? 1 : 0;
@@ -185,16 +185,31 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   ep.pq = pq;
   ep.run = nullptr;
   ep.q_in_epilogue = 1;
+  // Many draft rows: reduce q in its own stream before the LM head, which
+  // then skips its q-warps.
+  const bool q_stream = sample && dtype == SPECDEC_BF16 && B * gamma > kQWarpMaxRows;
+  ep.q_warps = q_stream ? 0 : 1;
+  int Pq = 0;
+  if (q_stream) {
+    if (launch_qstats(static_cast<const __nv_bfloat16*>(draft_logits), B * gamma, V, c, pq,
+                      stream) != cudaSuccess)
+      return SPECDEC_ERR_CUDA;
+    Pq = (V + kQChunk - 1) / kQChunk;
+  }
 
   if (ex.ev0 && cudaEventRecord(ex.ev0, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
   cudaError_t e;
   if (dtype == SPECDEC_BF16) {
-    const TcGeometry g = tc_geometry(pl.M, V, d, nsm);
+    const int max_clusters = tc_max_clusters(pl.M, V, d);
+    const TcGeometry g = tc_geometry(pl.M, V, d, nsm, max_clusters);
+    // With a cluster each CTA loads BT/K rows of every hidden slice.
+    const int h_rows = g.BT / g.K;
+    const int h_slices = g.K > 1 ? 1 : g.kc;
     CUtensorMap tw, th;
     const bool ok = g.box3d ? (encode_bf16_rows3d(&tw, W, V, d, kBlockV, g.kc) &&
-                               encode_bf16_rows3d(&th, hidden, pl.M, d, g.BT, g.kc))
+                               encode_bf16_rows3d(&th, hidden, pl.M, d, h_rows, h_slices))
                             : (encode_bf16_rows(&tw, W, V, d, kBlockV) &&
-                               encode_bf16_rows(&th, hidden, pl.M, d, g.BT));
+                               encode_bf16_rows(&th, hidden, pl.M, d, h_rows));
     if (!ok) return SPECDEC_ERR_CUDA;
     TcLaunch L;
     L.tmap_w = &tw;
@@ -206,6 +221,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
     L.status = status;
     L.fix = reinterpret_cast<float*>(ws + pl.off_fix);
     L.fix_tickets = reinterpret_cast<int*>(ws + pl.off_tickets);
+    L.max_clusters = max_clusters;
     L.ep = ep;
     P = g.records;
     e = launch_lmhead_tc(L, nsm, stream);
@@ -221,6 +237,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   A.gamma = gamma;
   A.V = V;
   A.P = P;
+  A.Pq = q_stream ? Pq : P;
   A.mode = mode;
   A.dl_bf16 = dtype == SPECDEC_BF16;
   A.c = c;

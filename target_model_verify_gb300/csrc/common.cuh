@@ -16,6 +16,8 @@ constexpr int kBlockK = 64;         // bf16 per 128-byte swizzled smem row
 constexpr int kMaxBT = 256;         // token rows per tile (MMA N) at most
 constexpr int kChunkV = 4096;       // residual-sampler chunk (256 threads x 16)
 constexpr int kMaxVocab = 1 << 22;  // V limit: the sampler stages 1024 chunk sums
+constexpr int kQChunk = 8192;       // draft-logit columns per q record (standalone stream)
+constexpr int kQWarpMaxRows = 16;   // draft rows up to which the LM-head q-warps reduce q
 constexpr int kSampleThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -214,6 +216,64 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
+// Multicast forms: the box lands at the same shared-memory offset in every
+// CTA of `mask` (this cluster) and completes bytes on each one's barrier.
+__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x,
+                                               int y, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x,
+                                               int y, int z, uint16_t mask, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(dst),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask), "l"(policy)
+      : "memory");
+}
+// Arrive on `bar` in every CTA of `mask` once this thread's MMAs are done.
+__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;" ::"r"(bar), "h"(mask)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.b32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// mbar_wait for a barrier that CTAs of the cluster arrive on.
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort, int* status) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  for (uint32_t n = 1;; ++n) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if ((n & 31u) == 0) {
+      if (*abort) return false;
+      if (globaltimer() - t0 > kWaitLimitNs) {
+        *abort = 1;
+        set_status(status, SPECDEC_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+
 // 3-D tiled TMA load of box {x.., y.., z..} into shared memory.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, uint32_t bar, int x,
                                             int y, int z, uint64_t policy) {
@@ -270,6 +330,25 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
   for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+}
+
+// 32 consecutive columns in one load.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, "
+      "%11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, "
+      "%28, %29, %30, %31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+        "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(r[k]);
 }
 
 // Shared-memory matrix descriptor of a K-major operand stored with the
@@ -449,6 +528,7 @@ struct EpiParams {
   RedSlot* run;            // shared memory [M]: fold tiles into one record per
                            // row and CTA (NULL: one record per row and tile)
   int q_in_epilogue;       // 1: the epilogue also reduces the draft logits
+  int q_warps;             // 1: the LM-head kernel's q-warps reduce them
 };
 
 __device__ __forceinline__ void redslot_merge(RedSlot& a, const RedSlot& o, float c) {
@@ -457,6 +537,14 @@ __device__ __forceinline__ void redslot_merge(RedSlot& a, const RedSlot& o, floa
   if (argmax_better(o.am, o.ai, a.am, a.ai)) {
     a.am = o.am;
     a.ai = o.ai;
+  }
+}
+
+__device__ __forceinline__ void partialp_merge(PartialP& a, const PartialP& o, float c) {
+  osm_merge(a.m, a.s, o.m, o.s, c);
+  if (argmax_better(o.amax_v, o.amax_i, a.amax_v, a.amax_i)) {
+    a.amax_v = o.amax_v;
+    a.amax_i = o.amax_i;
   }
 }
 

@@ -18,7 +18,8 @@ struct TcLaunch {
   int M, V, d, gamma;
   int* status;
   float* fix;                    // stream-K fix-up slots (tc_fix_floats floats)
-  int* fix_tickets;              // kMaxGrid + 1 ints, zero at launch
+  int* fix_tickets;              // kFixSlots ints, zero at launch
+  int max_clusters;              // co-resident clusters of the launch shape (0: unknown)
   EpiParams ep;
 };
 cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream);
@@ -27,9 +28,14 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
 cudaError_t launch_lmhead_f32(const float* hidden, const float* W, int d, const EpiParams& ep,
                               cudaStream_t stream);
 
+// q records straight from the draft logits: one (max, sum) per draft row
+// and kQChunk columns, at pq[row * ceil(V / kQChunk) + chunk].
+cudaError_t launch_qstats(const __nv_bfloat16* dl, int n_rows, int V, float c, PartialQ* pq,
+                          cudaStream_t stream);
+
 // Combine the partials, apply the acceptance rule, write the kept prefix.
 struct AcceptLaunch {
-  int B, gamma, V, P, mode, dl_bf16;
+  int B, gamma, V, P, Pq, mode, dl_bf16;   // P, Pq: records per p row and per q row
   float c;                       // log2(e) / T
   uint64_t seed;
   const PartialP* pp;
@@ -70,21 +76,27 @@ cudaError_t launch_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose,
 // Tile geometry and schedule of the tensor-core path, shared by the
 // workspace planner and the launcher.
 constexpr int kMaxGrid = 256;    // persistent CTAs at most (one per SM)
+constexpr int kFixSlots = kMaxGrid + 2;   // stream-K boundaries x cluster ranks
 struct TcGeometry {
   int BT;                        // token rows per tile: multiple of 16, <= 256
   int n_tt;                      // token tiles
   int kc;                        // 64-wide k slices per shared-memory stage
   int box3d;                     // 3-D boxes {64, rows, kc} (d % 64 == 0)
   int stages, stage_bytes, tmem_cols, smem_bytes;
+  int n_vt;                      // vocabulary tiles of 128
+  int K;                         // CTAs per cluster sharing hidden slices
   int n_units, nk, grid;
   int stream_k;                  // one token tile: contiguous k-iteration ranges
   int records;                   // partial records per row (grid or vocabulary tiles)
 };
-TcGeometry tc_geometry(int M, int V, int d, int num_sms);
+TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters);
+// Co-resident clusters of the kernel for this shape on the current device
+// (0 when the shape runs without clusters).
+int tc_max_clusters(int M, int V, int d);
 // Floats of stream-K fix-up storage for a shape (0 without stream-K).
 inline size_t tc_fix_floats(int M, int V, int d) {
-  const TcGeometry g = tc_geometry(M, V, d, kMaxGrid);
-  return g.stream_k ? (size_t)(kMaxGrid + 1) * 2 * g.BT * kBlockV : 0;
+  const TcGeometry g = tc_geometry(M, V, d, kMaxGrid, 0);
+  return g.stream_k ? (size_t)kFixSlots * 2 * g.BT * kBlockV : 0;
 }
 
 }  // namespace specdec

@@ -8,25 +8,33 @@
 //
 // Layout: swap-AB. The MMA's M dimension is a 128-row tile of W_lm (the
 // vocabulary), its N dimension the BT token rows, so z^T[v, m] lands in
-// tensor memory with one vocabulary row per TMEM lane. A work unit is a
-// (vocabulary tile, token tile) pair; its k dimension is nk k-steps, each
-// one shared-memory stage of C adjacent slices of 64 (C = 4 at small batch).
-// With d % 64 == 0 the loads are 3-D boxes {64, rows, C}, so each W row
-// contributes C*128 contiguous bytes per request: fewer, longer DRAM bursts,
+// tensor memory with one vocabulary row per TMEM lane. Each k-step is one
+// shared-memory stage of C adjacent 64-wide k-slices (C = 4 at small
+// batch). With d % 64 == 0 the loads are 3-D boxes {64, rows, C}, so each W
+// row gives C*128 contiguous bytes per request: fewer, longer DRAM bursts,
 // which measured ~7.1 TB/s against ~6.8 TB/s for one 128-byte slice per row.
 //
-// Scheduling, one persistent CTA per SM:
-//   * one token tile (M <= 256, every small-batch shape): stream-K. The
-//     n_units * nk (unit, k-step) iterations are cut into equal contiguous
-//     ranges, one per CTA, so every SM streams the same number of W bytes.
-//     A unit cut between two CTAs leaves each a partial accumulator; both
-//     write theirs to a fix-up slot and take an atomic ticket, and the
-//     second to arrive adds the two and runs the epilogue (nobody waits).
-//     Each CTA folds the softmax partials of all its tiles into one record
-//     per token row.
+// Clusters: with large token tiles (BT >= 64) every vocabulary tile would
+// re-read the token tile's hidden slices from L2 (up to twice the W bytes).
+// There, K = 2 CTAs form a cluster that works on neighbouring vocabulary
+// tiles in lockstep: each loads its own W tile and half of the shared
+// hidden slice, multicast into both CTAs' shared memory, and each MMA
+// thread releases a stage in both CTAs (multicast commit), so a stage is
+// refilled only once both have consumed it. K = 1 elsewhere.
+//
+// Scheduling, one persistent CTA per SM, in cluster units (K neighbouring
+// vocabulary tiles x one token tile; CTA rank r of the cluster takes tile
+// K*unit + r):
+//   * one token tile (M <= 256): stream-K. The units x k-steps iterations
+//     are cut into equal contiguous ranges, one per cluster, so every SM
+//     streams the same number of W bytes. A tile cut between two clusters
+//     leaves each CTA a partial accumulator; both write theirs to a fix-up
+//     slot and take an atomic ticket, and the second to arrive adds the two
+//     and runs the epilogue (nobody waits). Each CTA folds the softmax
+//     partials of all its tiles into one record per token row.
 //   * several token tiles: units dealt round-robin with the token tile
-//     fastest, so the CTAs that share a W tile run together and read it
-//     once from HBM and the rest from L2; one record per (row, tile).
+//     fastest, so the clusters that share W tiles run together and read
+//     them once from HBM and the rest from L2; one record per (row, tile).
 //
 // Warp roles (320 threads):
 //   warp 0     one thread issues TMA loads of W and hidden k-slices into a
@@ -38,10 +46,11 @@
 //   warps 6-9  q-warps: stream the draft logits of the same vocabulary tiles
 //              (8 rows in flight per warp) and reduce their softmax
 //              partials for q, off the epilogue's critical path. The CTA
-//              holding a unit's first k-step scores that unit's draft rows.
+//              holding a tile's first k-step scores that tile's draft rows.
 // Every wait is bounded (1 s); a timeout records SPECDEC_ERR_TIMEOUT, stops
 // the other roles, waits for copies and MMAs already issued, frees tensor
-// memory and returns.
+// memory and returns (a cluster partner's waits then run out as well, so
+// the closing cluster barrier is always reached).
 #include <cuda.h>
 
 #include "kernels.h"
@@ -56,40 +65,51 @@ constexpr int kMaxStagesC1 = 10;   // stage caps by slices per stage (measured)
 constexpr int kMaxStagesC2 = 4;
 constexpr int kMaxStagesC4 = 3;
 constexpr int kSmemLimit = 232448;               // 227 KB opt-in per CTA
-constexpr int kMiscBytes = 2048;   // mbarriers, flags and the 64 cross-warp slots
 constexpr unsigned long long kDrainLimitNs = 100000000ull;
-constexpr int kRunBytes = kMaxBT * (int)(sizeof(RedSlot) + sizeof(PartialQ));
+// Shared memory after the stages: mbarriers and flags (256 B), then per
+// token column of the tile: the four epilogue warps' partials, the CTA's
+// folded p record and its folded q record.
+__host__ __device__ constexpr int misc_bytes(int BT) {
+  return 256 + BT * (4 * (int)sizeof(PartialP) + (int)sizeof(PartialP) + (int)sizeof(PartialQ));
+}
 constexpr int kMaxDevices = 64;
+constexpr int kClusterMinBT = 64;  // token tiles from this size share hidden slices
 
 struct TcParams {
   int M, V, d, gamma;
-  int BT, n_tt, n_units, nk, stages;
+  int BT, n_tt, nk, stages;
+  int n_vt;                      // vocabulary tiles
+  int K;                         // CTAs per cluster (1 or 2)
+  int n_units;                   // cluster units: ceil(n_vt / K) * n_tt
   int kc;                        // 64-wide k slices per stage (C)
   int box3d;                     // 1: 3-D boxes {64, rows, C}; 0: 2-D boxes, C = 1
   int stream_k;                  // 1: contiguous iteration ranges (one token tile)
   long long total_iters;         // n_units * nk (k-steps)
   uint32_t stage_bytes, tmem_cols;
   int* status;
-  float* fix;                    // [(grid+1) * 2][BT * 128] partial accumulators
-  int* fix_tickets;              // [grid+1], zero at launch
+  float* fix;                    // [slots * 2][BT * 128] partial accumulators
+  int* fix_tickets;              // [slots], zero at launch
   EpiParams ep;
 };
 
-// One stretch of work: k-steps [kb, ke) of unit `unit`.
+// One stretch of work: k-steps [kb, ke) of cluster unit `unit`.
 struct Piece {
   int unit, kb, ke;
 };
 
-// The sequence of pieces a CTA processes; all three roles walk it alike.
+// The sequence of pieces a cluster processes; all roles of all its CTAs
+// walk it alike.
 struct PieceIter {
   long long it, end;
   int unit;
   __device__ PieceIter(const TcParams& p) {
+    const int cid = blockIdx.x / p.K;
+    const int ncl = gridDim.x / p.K;
     if (p.stream_k) {
-      it = p.total_iters * blockIdx.x / gridDim.x;
-      end = p.total_iters * (blockIdx.x + 1) / gridDim.x;
+      it = p.total_iters * cid / ncl;
+      end = p.total_iters * (cid + 1) / ncl;
     } else {
-      unit = blockIdx.x;
+      unit = cid;
     }
   }
   __device__ bool next(const TcParams& p, Piece& pc) {
@@ -107,7 +127,7 @@ struct PieceIter {
     pc.unit = unit;
     pc.kb = 0;
     pc.ke = p.nk;
-    unit += gridDim.x;
+    unit += gridDim.x / p.K;
     return true;
   }
 };
@@ -143,17 +163,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  RedSlot* red = reinterpret_cast<RedSlot*>(misc + 8 * (2 * S + 5) + 64);
-  RedSlot* run = red + 64;       // [BT] per-row records folded over the CTA's tiles
-  PartialQ* qrun = reinterpret_cast<PartialQ*>(run + kMaxBT);   // [BT] draft rows, likewise
+  PartialP* red = reinterpret_cast<PartialP*>(misc + 256);   // [4 warps][BT] column partials
+  PartialP* run = red + 4 * p.BT;  // [BT] per-row records folded over the CTA's tiles
+  PartialQ* qrun = reinterpret_cast<PartialQ*>(run + p.BT);  // [BT] draft rows, likewise
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rank = (int)(blockIdx.x % p.K);      // rank within the cluster
+  const int cid = (int)(blockIdx.x / p.K);
+  const uint16_t cmask = (uint16_t)((1u << p.K) - 1u);
+  const int hid_rows = p.BT / p.K;               // hidden rows this CTA loads per slice
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      mbar_init(empty_bar(s), p.K);             // one release per CTA of the cluster
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
@@ -165,12 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (p.stream_k)
     for (int r = threadIdx.x; r < p.BT; r += kThreads) {
-      run[r] = redslot_empty();
+      run[r] = PartialP{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
       qrun[r] = PartialQ{-INFINITY, 0.f};
     }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
   tc_fence_before();
   __syncthreads();
+  if (p.K > 1) cluster_sync_all();   // partners' barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -186,22 +211,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       PieceIter itr(p);
       Piece pc;
       while (ok && itr.next(p, pc)) {
-        const int vt = pc.unit / p.n_tt;
-        const int tt = pc.unit - vt * p.n_tt;
+        const int vt = (pc.unit / p.n_tt) * p.K + rank;
+        const int tt = pc.unit % p.n_tt;
         for (int kc = pc.kb; kc < pc.ke; ++kc) {
-          if (!mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status)) {
+          const bool got = p.K > 1 ? mbar_wait_cluster(empty_bar(s), ph ^ 1u, abort_flag, p.status)
+                                   : mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status);
+          if (!got) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(full_bar(s), p.stage_bytes);
           const uint32_t a = sbase + (uint32_t)s * p.stage_bytes;
           const uint32_t h = a + (uint32_t)(p.kc * kStageA);
-          if (p.box3d) {
+          if (p.box3d)
             tma_load_3d(a, &tmap_w, full_bar(s), 0, vt * kBlockV, kc * p.kc, pol_w);
-            tma_load_3d(h, &tmap_h, full_bar(s), 0, tt * p.BT, kc * p.kc, pol_h);
-          } else {
+          else
             tma_load_2d(a, &tmap_w, full_bar(s), kc * kBlockK, vt * kBlockV, pol_w);
-            tma_load_2d(h, &tmap_h, full_bar(s), kc * kBlockK, tt * p.BT, pol_h);
+          if (p.K == 1) {
+            if (p.box3d)
+              tma_load_3d(h, &tmap_h, full_bar(s), 0, tt * p.BT, kc * p.kc, pol_h);
+            else
+              tma_load_2d(h, &tmap_h, full_bar(s), kc * kBlockK, tt * p.BT, pol_h);
+          } else {
+            // This CTA's share of every slice: rows [rank*BT/K, (rank+1)*BT/K).
+            const int row = tt * p.BT + rank * hid_rows;
+            for (int c = 0; c < p.kc; ++c) {
+              const uint32_t dst =
+                  h + (uint32_t)(c * p.BT * kBlockK * 2 + rank * hid_rows * kBlockK * 2);
+              if (p.box3d)
+                tma_load_3d_mc(dst, &tmap_h, full_bar(s), 0, row, kc * p.kc + c, cmask, pol_h);
+              else
+                tma_load_2d_mc(dst, &tmap_h, full_bar(s), kc * kBlockK, row, cmask, pol_h);
+            }
           }
           issued_mask |= 1u << s;
           issued_phase = (issued_phase & ~(1u << s)) | (ph << s);
@@ -253,7 +294,10 @@ __global__ void __launch_bounds__(kThreads, 1)
               tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
                           (kc > pc.kb || c > 0 || k > 0) ? 1u : 0u);
           }
-          tc_commit(empty_bar(s));
+          if (p.K > 1)
+            tc_commit_mc(empty_bar(s), cmask);   // the stage is free in every partner too
+          else
+            tc_commit(empty_bar(s));
           if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -269,16 +313,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= 6) {
     // ---------------------------------------------------------- q-warps --
-    if (p.ep.sample) {
+    if (p.ep.sample && p.ep.q_warps) {
       const int qw = warp - 6;
       const int g1 = p.gamma + 1;
       const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(p.ep.dl);
       PieceIter itr(p);
       Piece pc;
       while (itr.next(p, pc)) {
-        if (pc.kb != 0) continue;
-        const int vt = pc.unit / p.n_tt;
-        const int tt = pc.unit - vt * p.n_tt;
+        const int vt = (pc.unit / p.n_tt) * p.K + rank;
+        if (pc.kb != 0 || vt >= p.n_vt) continue;
+        const int tt = pc.unit % p.n_tt;
         const int m_lo = tt * p.BT;
         const int m_hi = min(p.M, m_lo + p.BT);
         // Draft rows of token rows [m_lo, m_hi): a contiguous range.
@@ -334,9 +378,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int q = warp & 3;                 // TMEM lane quarter of this warp
     const int epi_tid = threadIdx.x - 64;
     const int row = q * 32 + lane;          // vocabulary row within the tile
-    EpiParams ep = p.ep;
-    ep.run = p.stream_k ? run : nullptr;
     const size_t slot_floats = (size_t)p.BT * kBlockV;
+    const bool vsample = p.ep.sample != 0;
+    const bool vargmax = p.ep.want_argmax != 0;
     int ul = 0;
     PieceIter itr(p);
     Piece pc;
@@ -344,8 +388,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int acc = ul & 1;
       const uint32_t aph = (uint32_t)(ul >> 1) & 1u;
       ++ul;
-      const int vt = pc.unit / p.n_tt;
-      const int tt = pc.unit - vt * p.n_tt;
+      const int vt = (pc.unit / p.n_tt) * p.K + rank;
+      const int tt = pc.unit % p.n_tt;
       const int v = vt * kBlockV + row;
       const int m_base = tt * p.BT;
       if (epi_tid == 0) *epi_flag = mbar_wait(tfull_bar(acc), aph, abort_flag, p.status) ? 1 : 0;
@@ -357,12 +401,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n_chunks = (min(p.BT, p.M - m_base) + 15) / 16;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.BT);
 
-      bool finish = true;
+      // A tile past the vocabulary (odd tile count in a cluster) has nothing to report.
+      bool finish = vt < p.n_vt;
       const float* other = nullptr;
-      if (pc.kb > 0 || pc.ke < p.nk) {
-        // A unit shared with a neighbouring CTA: the piece holding k-slice 0
-        // is part A of the boundary slot after its CTA, the other part B.
-        const int slot = pc.kb > 0 ? (int)blockIdx.x : (int)blockIdx.x + 1;
+      if (finish && (pc.kb > 0 || pc.ke < p.nk)) {
+        // A tile shared with the neighbouring cluster: the piece holding
+        // k-step 0 is part A of the boundary slot after its cluster, the
+        // other part B. Slots are per boundary and cluster rank.
+        const int bnd = pc.kb > 0 ? cid : cid + 1;
+        const int slot = bnd * p.K + rank;
         const int part = pc.kb > 0 ? 1 : 0;
         float* mine = p.fix + ((size_t)slot * 2 + part) * slot_floats;
         other = p.fix + ((size_t)slot * 2 + (1 - part)) * slot_floats;
@@ -385,19 +432,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (finish) __threadfence();
       }
       if (finish) {
-        float zq[16];   // draft logits are reduced by the q-warps
+        const bool vvalid = v < p.V;
+        // Per 16-column chunk: logits out, then each warp's (max, sum exp2)
+        // and argmax per column into red[warp quarter][column]. Two chunks
+        // per tensor-memory load.
+        for (int c = 0; c < n_chunks; c += 2) {
+          float accv[32];
+          const int nh = c + 1 < n_chunks ? 2 : 1;
+          if (nh == 2) {
+            tmem_ld32(tbase + (uint32_t)(c * 16), accv);
+          } else {
+            float a16[16];
+            tmem_ld16(tbase + (uint32_t)(c * 16), a16);
 #pragma unroll
-        for (int n = 0; n < 16; ++n) zq[n] = -INFINITY;
-        for (int c = 0; c < n_chunks; ++c) {
-          float accv[16];
-          tmem_ld16(tbase + (uint32_t)(c * 16), accv);
-          if (other != nullptr) {
-#pragma unroll
-            for (int n = 0; n < 16; ++n)
-              accv[n] += __ldcg(other + (size_t)(c * 16 + n) * kBlockV + row);
+            for (int n = 0; n < 16; ++n) accv[n] = a16[n];
           }
-          epilogue_chunk16<DL>(accv, zq, m_base + c * 16, v, vt, q, lane, epi_tid, red, ep, 1);
+          for (int h = 0; h < nh; ++h) {
+            const int cc = c + h;
+            float z[16];
+#pragma unroll
+            for (int n = 0; n < 16; ++n) z[n] = accv[h * 16 + n];
+            if (other != nullptr) {
+#pragma unroll
+              for (int n = 0; n < 16; ++n)
+                z[n] += __ldcg(other + (size_t)(cc * 16 + n) * kBlockV + row);
+            }
+            const int m0 = m_base + cc * 16;
+            if (p.ep.zout != nullptr && vvalid) {
+#pragma unroll
+              for (int n = 0; n < 16; ++n)
+                if (m0 + n < p.M) __stcs(p.ep.zout + (size_t)(m0 + n) * p.V + v, z[n]);
+            }
+            float zm[16];
+#pragma unroll
+            for (int n = 0; n < 16; ++n) zm[n] = vvalid ? z[n] : -INFINITY;
+            PartialP r{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+            if (vsample) warp_softmax16(zm, p.ep.c, r.m, r.s);
+            if (vargmax) warp_argmax16(zm, vvalid ? v : 0x7fffffff, r.amax_v, r.amax_i);
+            if ((lane & 1) == 0) red[q * p.BT + cc * 16 + (lane >> 1)] = r;
+          }
         }
+        named_bar_sync(1, 128);
+        // Columns across the four warp quarters, 128 columns at a time;
+        // column col is always folded by thread col % 128.
+        const int ncols = min(p.BT, p.M - m_base);
+        for (int col = epi_tid; col < ncols; col += 128) {
+          PartialP a = red[col];
+#pragma unroll
+          for (int qq = 1; qq < 4; ++qq) partialp_merge(a, red[qq * p.BT + col], p.ep.c);
+          const int m = m_base + col;
+          if (p.stream_k)
+            partialp_merge(run[m], a, p.ep.c);
+          else
+            p.ep.pp[(size_t)m * p.ep.P + vt] = a;
+        }
+        named_bar_sync(1, 128);
       }
       tc_fence_before();
       mbar_arrive(tempty_bar(acc));
@@ -405,11 +494,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (p.stream_k) {
       // One record per token row for everything this CTA finished.
       named_bar_sync(1, 128);
-      const int g1 = p.gamma + 1;
-      for (int m = epi_tid; m < p.M; m += 128) {
-        const RedSlot a = run[m];
-        p.ep.pp[(size_t)m * p.ep.P + blockIdx.x] = PartialP{a.pm, a.ps, a.am, a.ai};
-      }
+      for (int m = epi_tid; m < p.M; m += 128) p.ep.pp[(size_t)m * p.ep.P + blockIdx.x] = run[m];
     }
   }
 
@@ -419,11 +504,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, p.tmem_cols);
   }
+  // Partners may still arrive on this CTA's barriers until they finish.
+  if (p.K > 1) cluster_sync_all();
+}
+
+int max_clusters_cached(int smem_bytes, int K) {
+  static int cache[kMaxDevices][3] = {{0}};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
+  if (cache[dev][0] == smem_bytes && cache[dev][1] == K) return cache[dev][2];
+  auto kern = lmhead_tc_kernel<__nv_bfloat16>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
+      cudaSuccess)
+    return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(K * 512);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem_bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = K;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) n = 0;
+  cache[dev][0] = smem_bytes;
+  cache[dev][1] = K;
+  cache[dev][2] = n;
+  return n;
 }
 
 }  // namespace
 
-TcGeometry tc_geometry(int M, int V, int d, int num_sms) {
+TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters) {
   TcGeometry g;
   g.n_tt = (M + kMaxBT - 1) / kMaxBT;
   if (g.n_tt < 1) g.n_tt = 1;
@@ -433,7 +548,7 @@ TcGeometry tc_geometry(int M, int V, int d, int num_sms) {
   // Slices per stage: 4 while three such stages fit, else 2 while four fit,
   // else 1 (the stream rates these caps were chosen from are in the kernel
   // header comment).
-  const int budget = kSmemLimit - 1024 - kMiscBytes - kRunBytes;
+  const int budget = kSmemLimit - 1024 - misc_bytes(g.BT);
   const int slice_bytes = kStageA + g.BT * kBlockK * 2;
   g.box3d = d % kBlockK == 0 ? 1 : 0;
   if (g.box3d && budget / (4 * slice_bytes) >= 3) {
@@ -451,19 +566,30 @@ TcGeometry tc_geometry(int M, int V, int d, int num_sms) {
   int cols = 32;
   while (cols < 2 * g.BT) cols <<= 1;
   g.tmem_cols = cols;
-  g.smem_bytes = 1024 + g.stages * g.stage_bytes + kMiscBytes + kRunBytes;
-  const int n_vt = (V + kBlockV - 1) / kBlockV;
-  g.n_units = n_vt * g.n_tt;
+  g.smem_bytes = 1024 + g.stages * g.stage_bytes + misc_bytes(g.BT);
+  g.n_vt = (V + kBlockV - 1) / kBlockV;
+  g.K = (g.BT >= kClusterMinBT && g.n_vt >= 2) ? 2 : 1;
+  g.n_units = ((g.n_vt + g.K - 1) / g.K) * g.n_tt;
   g.nk = ((d + kBlockK - 1) / kBlockK + g.kc - 1) / g.kc;
-  int sms = num_sms < kMaxGrid ? num_sms : kMaxGrid;
-  g.grid = g.n_units < sms ? g.n_units : sms;
+  const int sms = num_sms < kMaxGrid ? num_sms : kMaxGrid;
+  int clusters = sms / g.K;
+  if (g.K > 1 && max_clusters > 0 && max_clusters < clusters) clusters = max_clusters;
+  if (clusters > g.n_units) clusters = g.n_units;
+  if (clusters < 1) clusters = 1;
+  g.grid = clusters * g.K;
   g.stream_k = g.n_tt == 1 ? 1 : 0;
-  g.records = g.stream_k ? g.grid : n_vt;
+  g.records = g.stream_k ? g.grid : g.n_vt;
   return g;
 }
 
+int tc_max_clusters(int M, int V, int d) {
+  const TcGeometry g = tc_geometry(M, V, d, kMaxGrid, 0);
+  if (g.K == 1) return 0;
+  return max_clusters_cached(g.smem_bytes, g.K);
+}
+
 cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream) {
-  const TcGeometry g = tc_geometry(L.M, L.V, L.d, num_sms);
+  const TcGeometry g = tc_geometry(L.M, L.V, L.d, num_sms, L.max_clusters);
   TcParams p;
   p.M = L.M;
   p.V = L.V;
@@ -471,11 +597,13 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   p.gamma = L.gamma;
   p.BT = g.BT;
   p.n_tt = g.n_tt;
-  p.n_units = g.n_units;
   p.nk = g.nk;
+  p.stages = g.stages;
+  p.n_vt = g.n_vt;
+  p.K = g.K;
+  p.n_units = g.n_units;
   p.kc = g.kc;
   p.box3d = g.box3d;
-  p.stages = g.stages;
   p.stream_k = g.stream_k;
   p.total_iters = (long long)g.n_units * g.nk;
   p.stage_bytes = (uint32_t)g.stage_bytes;
@@ -486,7 +614,7 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   p.ep = L.ep;
   p.ep.P = g.records;
   p.ep.run = nullptr;
-  p.ep.q_in_epilogue = 0;
+  p.ep.q_in_epilogue = 0;   // q-warps (ep.q_warps) or the standalone stream reduce q
   // The tensor-core path exists for bf16 inputs; draft logits share the dtype.
   auto kern = lmhead_tc_kernel<__nv_bfloat16>;
   // The shared-memory opt-in is set once per device and size.
@@ -499,8 +627,19 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < kMaxDevices) smem_set[dev] = g.smem_bytes;
   }
-  kern<<<g.grid, kThreads, g.smem_bytes, stream>>>(*L.tmap_w, *L.tmap_h, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(g.grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = g.smem_bytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = g.K;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, *L.tmap_w, *L.tmap_h, p);
 }
 
 }  // namespace specdec

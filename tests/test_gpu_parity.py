@@ -74,6 +74,9 @@ def test_tiny_fp32_sampling(seed):
     (60, 4, 128, 700, 1.3),     # M = 300: two token tiles of 160
     (1, 32, 192, 2049, 0.5),    # gamma at its maximum, ragged tail
     (7, 3, 8, 300, 1.0),        # d = 8: one zero-padded k-slice
+    (16, 4, 200, 2049, 0.9),    # M = 80: cluster pairs with 2-D boxes (d % 64 != 0), odd tile count
+    (16, 4, 128, 1920, 1.1),    # M = 80: cluster pairs with 3-D boxes, 15 tiles (one past the end)
+    (40, 4, 64, 3000, 1.0),     # M = 200: one token tile of 208, clusters, q from its own kernel
 ])
 def test_bf16_small_shapes(mode, B, gamma, d, V, T):
     w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, temperature=T, sigma=0.4)

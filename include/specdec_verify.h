@@ -184,6 +184,20 @@ int specdec_verify_noalloc(const void* hidden, const void* W_lm, const int32_t* 
 int specdec_read_status(const void* workspace, void* stream, int32_t* status);
 
 /*
+ * Self-test of the device-side failure detection: runs the LM-head kernel on
+ * a small internal shape with its loads withheld, so the first wait of the
+ * MMA stage finds a barrier that nothing will ever arm. The wait gives up
+ * after its bound (about 1 s), the kernel frees what it holds and returns,
+ * and *status receives the status word it left: SPECDEC_ERR_TIMEOUT when the
+ * detection works. Nothing faults, traps or hangs, and the CUDA context stays
+ * usable. Synchronises `stream`. workspace: at least
+ * specdec_verify_workspace_size(1, 4, 64, 256, SPECDEC_BF16, SPECDEC_GREEDY)
+ * bytes, 256-byte aligned; its contents are overwritten.
+ */
+int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream,
+                                  int32_t* status);
+
+/*
  * The library's own uniforms, for checking them against another
  * implementation: out[b*n_pos + i] = r (purpose 0) or u (purpose 1) for
  * sequence b < B and position i < n_pos. `out` is a device fp32 buffer.

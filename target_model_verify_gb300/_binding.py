@@ -49,6 +49,7 @@ _SIGNATURES = {
     "specdec_philox_uniforms": (_i, [_u64, _i, _i, _i, _vp, _vp]),
     "specdec_status_string": (ctypes.c_char_p, [_i]),
     "specdec_verify_noalloc": (_i, _CORE[:14] + [_vp]),
+    "specdec_selftest_wait_timeout": (_i, [_vp, _sz, _vp, ctypes.POINTER(ctypes.c_int32)]),
 }
 
 _lib = None
@@ -129,6 +130,14 @@ def specdec_read_status(workspace_ptr: int, stream_ptr: int) -> int:
     st = ctypes.c_int32(0)
     _check(lib().specdec_read_status(workspace_ptr, stream_ptr, ctypes.byref(st)),
            "specdec_read_status")
+    return int(st.value)
+
+
+def specdec_selftest_wait_timeout(workspace_ptr: int, workspace_bytes: int, stream_ptr: int) -> int:
+    """Runs the bounded-wait self-test; returns the status word it left."""
+    st = ctypes.c_int32(0)
+    _check(lib().specdec_selftest_wait_timeout(workspace_ptr, workspace_bytes, stream_ptr,
+                                               ctypes.byref(st)), "specdec_selftest_wait_timeout")
     return int(st.value)
 
 

@@ -222,6 +222,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
     L.fix = reinterpret_cast<float*>(ws + pl.off_fix);
     L.fix_tickets = reinterpret_cast<int*>(ws + pl.off_tickets);
     L.max_clusters = max_clusters;
+    L.withhold_loads = 0;
     L.ep = ep;
     P = g.records;
     e = launch_lmhead_tc(L, nsm, stream);
@@ -390,6 +391,59 @@ int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t
           cudaSuccess)
     return SPECDEC_ERR_CUDA;
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  return SPECDEC_OK;
+}
+
+int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void* stream_ptr,
+                                  int32_t* status) {
+  // A small sampling-free shape: M = 5 rows, V = 256, d = 64.
+  const int B = 1, gamma = 4, d = 64, V = 256;
+  if (!workspace || !status || ((uintptr_t)workspace % kAlign) != 0) return SPECDEC_ERR_INVALID_ARG;
+  const Plan pl = make_plan(B, gamma, d, V, SPECDEC_BF16, SPECDEC_GREEDY);
+  if (workspace_bytes < pl.total) return SPECDEC_ERR_WORKSPACE;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SPECDEC_ERR_CUDA;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  if (cudaMemsetAsync(ws, 0, pl.zeroed, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  const TcGeometry g = tc_geometry(pl.M, V, d, nsm, 0);
+  // The tensor maps point at the workspace; no load is ever issued through them.
+  CUtensorMap tw, th;
+  if (!encode_bf16_rows3d(&tw, ws, V, d, kBlockV, g.kc) ||
+      !encode_bf16_rows3d(&th, ws, pl.M, d, g.BT, g.kc))
+    return SPECDEC_ERR_CUDA;
+  EpiParams ep;
+  ep.M = pl.M;
+  ep.V = V;
+  ep.gamma = gamma;
+  ep.P = pl.P;
+  ep.c = kLog2e;
+  ep.sample = 0;
+  ep.want_argmax = 0;
+  ep.zout = nullptr;
+  ep.dl = nullptr;
+  ep.pp = reinterpret_cast<PartialP*>(ws + pl.off_pp);
+  ep.pq = reinterpret_cast<PartialQ*>(ws + pl.off_pq);
+  ep.run = nullptr;
+  ep.q_in_epilogue = 0;
+  ep.q_warps = 0;
+  TcLaunch L;
+  L.tmap_w = &tw;
+  L.tmap_h = &th;
+  L.M = pl.M;
+  L.V = V;
+  L.d = d;
+  L.gamma = gamma;
+  L.status = reinterpret_cast<int*>(ws);
+  L.fix = reinterpret_cast<float*>(ws + pl.off_fix);
+  L.fix_tickets = reinterpret_cast<int*>(ws + pl.off_tickets);
+  L.max_clusters = 0;
+  L.withhold_loads = 1;
+  L.ep = ep;
+  if (launch_lmhead_tc(L, nsm, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  if (cudaMemcpy(status, ws, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SPECDEC_ERR_CUDA;
   return SPECDEC_OK;
 }
 

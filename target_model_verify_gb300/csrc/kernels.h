@@ -20,6 +20,7 @@ struct TcLaunch {
   float* fix;                    // stream-K fix-up slots (tc_fix_floats floats)
   int* fix_tickets;              // kFixSlots ints, zero at launch
   int max_clusters;              // co-resident clusters of the launch shape (0: unknown)
+  int withhold_loads;            // self-test of the bounded waits (normally 0)
   EpiParams ep;
 };
 cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream);

@@ -89,6 +89,7 @@ struct TcParams {
   int* status;
   float* fix;                    // [slots * 2][BT * 128] partial accumulators
   int* fix_tickets;              // [slots], zero at launch
+  int withhold_loads;            // self-test: issue no loads, so the first wait runs out
   EpiParams ep;
 };
 
@@ -210,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       PieceIter itr(p);
       Piece pc;
-      while (ok && itr.next(p, pc)) {
+      while (ok && !p.withhold_loads && itr.next(p, pc)) {
         const int vt = (pc.unit / p.n_tt) * p.K + rank;
         const int tt = pc.unit % p.n_tt;
         for (int kc = pc.kb; kc < pc.ke; ++kc) {
@@ -611,6 +612,7 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   p.status = L.status;
   p.fix = L.fix;
   p.fix_tickets = L.fix_tickets;
+  p.withhold_loads = L.withhold_loads;
   p.ep = L.ep;
   p.ep.P = g.records;
   p.ep.run = nullptr;

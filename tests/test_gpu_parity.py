@@ -230,3 +230,22 @@ def test_chi_square_committed_token_law():
     assert stats.chisquare(counts, p0 * n).pvalue > 1e-4
     alpha = np.minimum(p0, q0).sum()
     assert abs(kept / n - alpha) < 4 * math.sqrt(alpha * (1 - alpha) / n)
+
+
+def test_bounded_wait_reports_timeout_and_context_survives():
+    """Failure detection without a fault: a wait on a barrier nothing arms
+    runs out after its bound, the kernel reports SPECDEC_ERR_TIMEOUT through
+    the status word, and the next verify call on the same context is exact."""
+    import time
+
+    import target_model_verify_gb300 as tv
+    b = tv._b
+    n = b.specdec_verify_workspace_size(1, 4, 64, 256, b.SPECDEC_BF16, b.SPECDEC_GREEDY)
+    ws = torch.empty(n, dtype=torch.uint8, device=DEV)
+    t0 = time.time()
+    st = b.specdec_selftest_wait_timeout(ws.data_ptr(), n, torch.cuda.current_stream().cuda_stream)
+    dt = time.time() - t0
+    assert st == b.SPECDEC_ERR_TIMEOUT
+    assert 0.5 < dt < 30
+    w, inp = _gen("llama3_8b_head", 8, B=2, V=1500, d=256)
+    _full_check(w, inp, 2, ov.SAMPLE)

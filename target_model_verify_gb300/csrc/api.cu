@@ -5,6 +5,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <atomic>
+#include <chrono>
 #include <cmath>
 #include <mutex>
 
@@ -21,7 +23,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Plan {
   int M, P, nchunks;
   size_t off_tickets, off_sel, off_counters, off_pp, off_pq, off_z, off_chunks, off_fix, total;
-  size_t zeroed;                 // bytes from the start cleared by every call
+
 };
 
 // Checks the shape; returns SPECDEC_OK or an error code.
@@ -45,8 +47,7 @@ Plan make_plan(int B, int gamma, int d, int V, int dtype, int mode) {
   const bool sample = mode == SPECDEC_SAMPLE;
   size_t off = align_up(sizeof(WsHeader));
   p.off_tickets = off;
-  off = align_up(off + sizeof(int) * kFixSlots);
-  p.zeroed = off;
+  off = align_up(off + sizeof(unsigned long long) * kFixSlots);
   p.off_sel = off;
   off = align_up(off + sizeof(SelectedRow) * (size_t)B);
   p.off_counters = off;
@@ -166,9 +167,10 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   float* chunk_sums = reinterpret_cast<float*>(ws + pl.off_chunks);
   const float c = sample ? kLog2e / T : kLog2e;
 
-  // The status word and the fix-up tickets are cleared by the call's first
-  // operation.
-  if (cudaMemsetAsync(status, 0, pl.zeroed, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  // Nothing is cleared up front: the LM-head kernel resets the status word
+  // after its dependency wait, and fix-up tickets are tagged with this call's
+  // epoch, so every kernel of the step can launch as a programmatic dependent.
+  const unsigned long long epoch = next_call_epoch();
   int P = (V + kBlockV - 1) / kBlockV;   // records per row written by the fp32 kernel
 
   EpiParams ep;
@@ -220,7 +222,8 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
     L.gamma = gamma;
     L.status = status;
     L.fix = reinterpret_cast<float*>(ws + pl.off_fix);
-    L.fix_tickets = reinterpret_cast<int*>(ws + pl.off_tickets);
+    L.fix_tickets = reinterpret_cast<unsigned long long*>(ws + pl.off_tickets);
+    L.epoch = epoch;
     L.max_clusters = max_clusters;
     L.withhold_loads = 0;
     L.ep = ep;
@@ -228,7 +231,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
     e = launch_lmhead_tc(L, nsm, stream);
   } else {
     e = launch_lmhead_f32(static_cast<const float*>(hidden), static_cast<const float*>(W), d, ep,
-                          stream);
+                          status, stream);
   }
   if (e != cudaSuccess) return SPECDEC_ERR_CUDA;
   if (ex.ev1 && cudaEventRecord(ex.ev1, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
@@ -291,6 +294,17 @@ size_t host_staging_bytes(int B, int gamma, int d, int V, int dtype, int mode) {
 }
 
 }  // namespace
+
+namespace specdec {
+unsigned long long next_call_epoch() {
+  // Starts from the clock so that tags left in reused memory by another
+  // process are unlikely to match; then strictly increasing.
+  static std::atomic<unsigned long long> counter{
+      (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count() |
+      (1ull << 63)};
+  return counter.fetch_add(1, std::memory_order_relaxed);
+}
+}  // namespace specdec
 
 extern "C" {
 
@@ -405,7 +419,6 @@ int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void*
   if (nsm <= 0) return SPECDEC_ERR_CUDA;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   char* ws = static_cast<char*>(workspace);
-  if (cudaMemsetAsync(ws, 0, pl.zeroed, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
   const TcGeometry g = tc_geometry(pl.M, V, d, nsm, 0);
   // The tensor maps point at the workspace; no load is ever issued through them.
   CUtensorMap tw, th;
@@ -436,7 +449,8 @@ int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void*
   L.gamma = gamma;
   L.status = reinterpret_cast<int*>(ws);
   L.fix = reinterpret_cast<float*>(ws + pl.off_fix);
-  L.fix_tickets = reinterpret_cast<int*>(ws + pl.off_tickets);
+  L.fix_tickets = reinterpret_cast<unsigned long long*>(ws + pl.off_tickets);
+  L.epoch = next_call_epoch();
   L.max_clusters = 0;
   L.withhold_loads = 1;
   L.ep = ep;

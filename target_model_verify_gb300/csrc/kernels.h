@@ -18,7 +18,8 @@ struct TcLaunch {
   int M, V, d, gamma;
   int* status;
   float* fix;                    // stream-K fix-up slots (tc_fix_floats floats)
-  int* fix_tickets;              // kFixSlots ints, zero at launch
+  unsigned long long* fix_tickets;   // kFixSlots tags, any initial contents
+  unsigned long long epoch;      // per-call tag (next_call_epoch)
   int max_clusters;              // co-resident clusters of the launch shape (0: unknown)
   int withhold_loads;            // self-test of the bounded waits (normally 0)
   EpiParams ep;
@@ -27,7 +28,10 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
 
 // The same scoring for fp32 inputs on the CUDA cores.
 cudaError_t launch_lmhead_f32(const float* hidden, const float* W, int d, const EpiParams& ep,
-                              cudaStream_t stream);
+                              int* status, cudaStream_t stream);
+
+// A tag that no earlier call in this process used.
+unsigned long long next_call_epoch();
 
 // q records straight from the draft logits: one (max, sum) per draft row
 // and kQChunk columns, at pq[row * ceil(V / kQChunk) + chunk].

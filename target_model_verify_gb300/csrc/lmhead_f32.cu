@@ -15,7 +15,9 @@ constexpr int kKSlice = 32;
 
 __global__ void __launch_bounds__(128)
     lmhead_f32_kernel(const float* __restrict__ H, const float* __restrict__ W, int d,
-                      const EpiParams ep) {
+                      const EpiParams ep, int* status) {
+  grid_dependency_wait();
+  if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *(volatile int*)status = SPECDEC_OK;
   __shared__ float ws[kKSlice][kBlockV + 1];
   __shared__ float hs[16][kKSlice];
   __shared__ RedSlot red[64];
@@ -55,10 +57,17 @@ __global__ void __launch_bounds__(128)
 }  // namespace
 
 cudaError_t launch_lmhead_f32(const float* hidden, const float* W, int d, const EpiParams& ep,
-                              cudaStream_t stream) {
-  const dim3 grid((ep.V + kBlockV - 1) / kBlockV, (ep.M + 15) / 16);
-  lmhead_f32_kernel<<<grid, 128, 0, stream>>>(hidden, W, d, ep);
-  return cudaGetLastError();
+                              int* status, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((ep.V + kBlockV - 1) / kBlockV, (ep.M + 15) / 16);
+  cfg.blockDim = dim3(128);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, lmhead_f32_kernel, hidden, W, d, ep, status);
 }
 
 }  // namespace specdec

@@ -88,7 +88,8 @@ struct TcParams {
   uint32_t stage_bytes, tmem_cols;
   int* status;
   float* fix;                    // [slots * 2][BT * 128] partial accumulators
-  int* fix_tickets;              // [slots], zero at launch
+  unsigned long long* fix_tickets;   // [slots]: epoch of the last part to arrive
+  unsigned long long epoch;      // this call's tag (never repeats within a process)
   int withhold_loads;            // self-test: issue no loads, so the first wait runs out
   EpiParams ep;
 };
@@ -194,6 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       qrun[r] = PartialQ{-INFINITY, 0.f};
     }
   if (warp == 1) tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+  // Launched with programmatic dependent launch: the set-up above overlaps
+  // the previous kernel; global memory is touched only after this wait.
+  grid_dependency_wait();
+  if (blockIdx.x == 0 && threadIdx.x == 0) *(volatile int*)p.status = SPECDEC_OK;
   tc_fence_before();
   __syncthreads();
   if (p.K > 1) cluster_sync_all();   // partners' barriers exist before any multicast
@@ -423,9 +428,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         named_bar_sync(1, 128);
         if (epi_tid == 0) {
-          const int ticket = atomicAdd(p.fix_tickets + slot, 1);
+          // The part that finds this call's epoch already there arrives second.
+          const unsigned long long prev = atomicExch(p.fix_tickets + slot, p.epoch);
           __threadfence();
-          *epi_flag = ticket == 1 ? 1 : 0;
+          *epi_flag = prev == p.epoch ? 1 : 0;
         }
         named_bar_sync(1, 128);
         finish = *epi_flag != 0;
@@ -612,6 +618,7 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   p.status = L.status;
   p.fix = L.fix;
   p.fix_tickets = L.fix_tickets;
+  p.epoch = L.epoch;
   p.withhold_loads = L.withhold_loads;
   p.ep = L.ep;
   p.ep.P = g.records;
@@ -634,13 +641,15 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = g.smem_bytes;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = g.K;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, kern, *L.tmap_w, *L.tmap_h, p);
 }
 

@@ -40,6 +40,7 @@ __global__ void __launch_bounds__(kThreads) qstats_kernel(const __nv_bfloat16* _
                                                           int n_rows, int V, float c,
                                                           PartialQ* __restrict__ pq, int Pq,
                                                           int vec_ok) {
+  grid_dependency_wait();   // programmatic dependent launch: inputs are ready after this
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = blockIdx.x * (kThreads / 32) + warp;
   if (r >= n_rows) return;
@@ -86,9 +87,16 @@ cudaError_t launch_qstats(const __nv_bfloat16* dl, int n_rows, int V, float c, P
                           cudaStream_t stream) {
   const int n_chunks = (V + kCols - 1) / kCols;
   const int vec_ok = (V % 8 == 0 && ((uintptr_t)dl & 15u) == 0) ? 1 : 0;
-  const dim3 grid((n_rows + kThreads / 32 - 1) / (kThreads / 32), n_chunks);
-  qstats_kernel<<<grid, kThreads, 0, stream>>>(dl, n_rows, V, c, pq, n_chunks, vec_ok);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((n_rows + kThreads / 32 - 1) / (kThreads / 32), n_chunks);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, qstats_kernel, dl, n_rows, V, c, pq, n_chunks, vec_ok);
 }
 
 }  // namespace specdec

@@ -204,9 +204,9 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   if (dtype == SPECDEC_BF16) {
     const int max_clusters = tc_max_clusters(pl.M, V, d);
     const TcGeometry g = tc_geometry(pl.M, V, d, nsm, max_clusters);
-    // With a cluster each CTA loads BT/K rows of every hidden slice.
+    // A CTA of a pair loads its BT/K token rows of all kc slices of a stage.
     const int h_rows = g.BT / g.K;
-    const int h_slices = g.K > 1 ? 1 : g.kc;
+    const int h_slices = g.kc;
     CUtensorMap tw, th;
     const bool ok = g.box3d ? (encode_bf16_rows3d(&tw, W, V, d, kBlockV, g.kc) &&
                                encode_bf16_rows3d(&th, hidden, pl.M, d, h_rows, h_slices))

@@ -216,30 +216,69 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, uint
       : "memory");
 }
 
-// Multicast forms: the box lands at the same shared-memory offset in every
-// CTA of `mask` (this cluster) and completes bytes on each one's barrier.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x,
-                                               int y, uint16_t mask, uint64_t policy) {
+// CTA-pair (2-SM) tcgen05 forms. One warp in each CTA of the pair allocates
+// collectively and both CTAs get the same tensor-memory address; an MMA
+// issued by the pair's leader with M = 256 reads A as two 128-row halves,
+// one in each CTA's shared memory at the same offset, and B as two halves
+// of its N rows likewise, and writes each CTA's 128 rows of D into that
+// CTA's tensor memory.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc2_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5, %6;" ::"r"(dst),
-      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(bar), "h"(mask), "l"(policy)
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_3d_mc(uint32_t dst, const void* tmap, uint32_t bar, int x,
-                                               int y, int z, uint16_t mask, uint64_t policy) {
+// TMA loads of a CTA pair: the box lands in this CTA's shared memory and its
+// bytes complete on `bar_cluster`, a barrier of either CTA of the pair (the
+// leader's, so one barrier counts both halves of a stage).
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
+                                                 uint32_t bar_cluster, int x, int y,
+                                                 uint64_t policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6, %7;" ::"r"(dst),
-      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(bar), "h"(mask), "l"(policy)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(bar_cluster), "l"(policy)
       : "memory");
 }
-// Arrive on `bar` in every CTA of `mask` once this thread's MMAs are done.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t mask) {
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
+                                                 uint32_t bar_cluster, int x, int y, int z,
+                                                 uint64_t policy) {
   asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.tile"
+      ".mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"((uint64_t)tmap), "r"(x), "r"(y), "r"(z), "r"(bar_cluster), "l"(policy)
+      : "memory");
+}
+// Arrive on `bar` in every CTA of `mask` once the pair MMAs issued so far are done.
+__device__ __forceinline__ void tc2_commit_mc(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(bar), "h"(mask)
       : "memory");
+}
+// The shared::cluster address of `addr` in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// Arrive on an mbarrier of another CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+               : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -394,16 +433,12 @@ __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
 // Online-softmax pair merge with one exp2: (ma, sa) <- (ma, sa) + (mb, sb),
 // s = sum of exp2((x - m) * c).
 __device__ __forceinline__ void osm_merge(float& ma, float& sa, float mb, float sb, float c) {
+  // Branch-free: scale the smaller side's sum by exp2(-|ma - mb| c).
   const float mm = fmaxf(ma, mb);
-  if (mm == -INFINITY) {
-    ma = mm;
-    sa = 0.f;
-    return;
-  }
-  if (ma >= mb)
-    sa = sa + sb * exp2f((mb - ma) * c);
-  else
-    sa = sb + sa * exp2f((ma - mb) * c);
+  const bool a_big = ma >= mb;
+  const float e = exp2f(-fabsf(ma - mb) * c);
+  const float s = fmaf(a_big ? sb : sa, e, a_big ? sa : sb);
+  sa = mm == -INFINITY ? 0.f : s;   // both empty (the exponent is NaN then)
   ma = mm;
 }
 

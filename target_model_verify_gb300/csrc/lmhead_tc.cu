@@ -14,13 +14,17 @@
 // row gives C*128 contiguous bytes per request: fewer, longer DRAM bursts,
 // which measured ~7.1 TB/s against ~6.8 TB/s for one 128-byte slice per row.
 //
-// Clusters: with large token tiles (BT >= 64) every vocabulary tile would
-// re-read the token tile's hidden slices from L2 (up to twice the W bytes).
-// There, K = 2 CTAs form a cluster that works on neighbouring vocabulary
-// tiles in lockstep: each loads its own W tile and half of the shared
-// hidden slice, multicast into both CTAs' shared memory, and each MMA
-// thread releases a stage in both CTAs (multicast commit), so a stage is
-// refilled only once both have consumed it. K = 1 elsewhere.
+// CTA pairs: with large token tiles (BT >= 64) each SM would have to take in
+// the whole token slice for every 128-row W slice (up to twice the W
+// bytes), and that ingress, not DRAM, limited the kernel. There K = 2 CTAs
+// form a cluster and run the 2-SM MMA (tcgen05.mma.cta_group::2, M = 256):
+// each CTA loads its own W tile (128 vocabulary rows) and only its half of
+// the token rows, and both CTAs' loads complete on the leader's (rank 0)
+// barrier, so the leader issues the MMA as soon as both halves of a stage
+// have landed and frees the stage in both CTAs with one multicast commit;
+// each CTA's tensor memory receives its 128 rows x BT accumulator. The
+// peer's epilogue releases an accumulator by arriving on the leader's
+// barrier. K = 1 elsewhere.
 //
 // Scheduling, one persistent CTA per SM, in cluster units (K neighbouring
 // vocabulary tiles x one token tile; CTA rank r of the cluster takes tile
@@ -36,14 +40,15 @@
 //     fastest, so the clusters that share W tiles run together and read
 //     them once from HBM and the rest from L2; one record per (row, tile).
 //
-// Warp roles (320 threads):
+// Warp roles (448 threads):
 //   warp 0     one thread issues TMA loads of W and hidden k-slices into a
 //              ring of shared-memory stages (full/empty mbarriers).
 //   warp 1     allocates tensor memory; one thread issues tcgen05.mma into
 //              one of two TMEM accumulators and commits to mbarriers.
-//   warps 2-5  epilogue: tcgen05.ld of the accumulator, fp32 logits out,
-//              softmax / argmax partials for p.
-//   warps 6-9  q-warps: stream the draft logits of the same vocabulary tiles
+//   warps 2-9  epilogue, two groups of four (one warp per TMEM lane quarter
+//              in each) taking alternate 32-column chunks: tcgen05.ld of the
+//              accumulator, fp32 logits out, softmax / argmax partials for p.
+//   warps 10-13 q-warps: stream the draft logits of the same vocabulary tiles
 //              (8 rows in flight per warp) and reduce their softmax
 //              partials for q, off the epilogue's critical path. The CTA
 //              holding a tile's first k-step scores that tile's draft rows.
@@ -58,7 +63,9 @@
 namespace specdec {
 namespace {
 
-constexpr int kThreads = 320;
+constexpr int kThreads = 448;
+constexpr int kEpiThreads = 256;   // warps 2-9
+constexpr int kQWarp0 = 10;        // first q-warp
 constexpr int kQRowsInFlight = 8;
 constexpr int kStageA = kBlockV * kBlockK * 2;   // 16 KB of W per stage
 constexpr int kMaxStagesC1 = 10;   // stage caps by slices per stage (measured)
@@ -66,11 +73,12 @@ constexpr int kMaxStagesC2 = 4;
 constexpr int kMaxStagesC4 = 3;
 constexpr int kSmemLimit = 232448;               // 227 KB opt-in per CTA
 constexpr unsigned long long kDrainLimitNs = 100000000ull;
-// Shared memory after the stages: mbarriers and flags (256 B), then per
+// Shared memory after the stages: mbarriers and flags (512 B), then per
 // token column of the tile: the four epilogue warps' partials, the CTA's
 // folded p record and its folded q record.
+constexpr int kBarBytes = 512;
 __host__ __device__ constexpr int misc_bytes(int BT) {
-  return 256 + BT * (4 * (int)sizeof(PartialP) + (int)sizeof(PartialP) + (int)sizeof(PartialQ));
+  return kBarBytes + BT * (4 * (int)sizeof(PartialP) + (int)sizeof(PartialP) + (int)sizeof(PartialQ));
 }
 constexpr int kMaxDevices = 64;
 constexpr int kClusterMinBT = 64;  // token tiles from this size share hidden slices
@@ -79,7 +87,7 @@ struct TcParams {
   int M, V, d, gamma;
   int BT, n_tt, nk, stages;
   int n_vt;                      // vocabulary tiles
-  int K;                         // CTAs per cluster (1 or 2)
+  int K;                         // CTAs per cluster (1, or 2 for the 2-SM MMA)
   int n_units;                   // cluster units: ceil(n_vt / K) * n_tt
   int kc;                        // 64-wide k slices per stage (C)
   int box3d;                     // 1: 3-D boxes {64, rows, C}; 0: 2-D boxes, C = 1
@@ -142,7 +150,9 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   return true;
 }
 
-template <typename DL>
+// kPair: the 2-SM (CTA pair) build; cta_group::1 and ::2 instructions cannot
+// share a kernel.
+template <typename DL, bool kPair>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
                      const __grid_constant__ CUtensorMap tmap_h, const TcParams p) {
@@ -162,10 +172,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * S + a); };
   auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * S + 2 + a); };
   const uint32_t mma_done_bar = bar0 + 8u * (2 * S + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (2 * S + 5));
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(misc + 8 * (3 * S + 5));
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* epi_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  PartialP* red = reinterpret_cast<PartialP*>(misc + 256);   // [4 warps][BT] column partials
+  PartialP* red = reinterpret_cast<PartialP*>(misc + kBarBytes);   // [4 warps][BT] column partials
   PartialP* run = red + 4 * p.BT;  // [BT] per-row records folded over the CTA's tiles
   PartialQ* qrun = reinterpret_cast<PartialQ*>(run + p.BT);  // [BT] draft rows, likewise
 
@@ -173,17 +183,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   const int rank = (int)(blockIdx.x % p.K);      // rank within the cluster
   const int cid = (int)(blockIdx.x / p.K);
-  const uint16_t cmask = (uint16_t)((1u << p.K) - 1u);
-  const int hid_rows = p.BT / p.K;               // hidden rows this CTA loads per slice
+  constexpr bool pair = kPair;
+  const int hid_rows = p.BT / p.K;               // token rows this CTA loads per slice
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), p.K);             // one release per CTA of the cluster
+      mbar_init(empty_bar(s), 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), 128);
+      mbar_init(tempty_bar(a), pair ? 2 * kEpiThreads : kEpiThreads);   // a pair's leader counts both epilogues
     }
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
@@ -194,14 +204,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       run[r] = PartialP{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
       qrun[r] = PartialQ{-INFINITY, 0.f};
     }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+  if (warp == 1) {
+    if constexpr (kPair)
+      tmem_alloc_pair(smem_u32(tmem_slot), p.tmem_cols);
+    else
+      tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+  }
   // Launched with programmatic dependent launch: the set-up above overlaps
   // the previous kernel; global memory is touched only after this wait.
   grid_dependency_wait();
   if (blockIdx.x == 0 && threadIdx.x == 0) *(volatile int*)p.status = SPECDEC_OK;
   tc_fence_before();
   __syncthreads();
-  if (p.K > 1) cluster_sync_all();   // partners' barriers exist before any multicast
+  if (pair) cluster_sync_all();   // the partner's barriers exist before any remote arrive
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -220,34 +235,35 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vt = (pc.unit / p.n_tt) * p.K + rank;
         const int tt = pc.unit % p.n_tt;
         for (int kc = pc.kb; kc < pc.ke; ++kc) {
-          const bool got = p.K > 1 ? mbar_wait_cluster(empty_bar(s), ph ^ 1u, abort_flag, p.status)
-                                   : mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status);
+          const bool got = pair ? mbar_wait_cluster(empty_bar(s), ph ^ 1u, abort_flag, p.status)
+                                : mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status);
           if (!got) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(full_bar(s), p.stage_bytes);
           const uint32_t a = sbase + (uint32_t)s * p.stage_bytes;
           const uint32_t h = a + (uint32_t)(p.kc * kStageA);
-          if (p.box3d)
-            tma_load_3d(a, &tmap_w, full_bar(s), 0, vt * kBlockV, kc * p.kc, pol_w);
-          else
-            tma_load_2d(a, &tmap_w, full_bar(s), kc * kBlockK, vt * kBlockV, pol_w);
-          if (p.K == 1) {
-            if (p.box3d)
-              tma_load_3d(h, &tmap_h, full_bar(s), 0, tt * p.BT, kc * p.kc, pol_h);
-            else
-              tma_load_2d(h, &tmap_h, full_bar(s), kc * kBlockK, tt * p.BT, pol_h);
+          // Token rows [rank*BT/K, (rank+1)*BT/K) of the tile (all of them when K = 1).
+          const int row = tt * p.BT + rank * hid_rows;
+          if constexpr (kPair) {
+            // Both halves of the stage complete on the leader's full barrier.
+            const uint32_t lead_full = mapa_shared(full_bar(s), 0);
+            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2u * p.stage_bytes);
+            if (p.box3d) {
+              tma_load_3d_pair(a, &tmap_w, lead_full, 0, vt * kBlockV, kc * p.kc, pol_w);
+              tma_load_3d_pair(h, &tmap_h, lead_full, 0, row, kc * p.kc, pol_h);
+            } else {
+              tma_load_2d_pair(a, &tmap_w, lead_full, kc * kBlockK, vt * kBlockV, pol_w);
+              tma_load_2d_pair(h, &tmap_h, lead_full, kc * kBlockK, row, pol_h);
+            }
           } else {
-            // This CTA's share of every slice: rows [rank*BT/K, (rank+1)*BT/K).
-            const int row = tt * p.BT + rank * hid_rows;
-            for (int c = 0; c < p.kc; ++c) {
-              const uint32_t dst =
-                  h + (uint32_t)(c * p.BT * kBlockK * 2 + rank * hid_rows * kBlockK * 2);
-              if (p.box3d)
-                tma_load_3d_mc(dst, &tmap_h, full_bar(s), 0, row, kc * p.kc + c, cmask, pol_h);
-              else
-                tma_load_2d_mc(dst, &tmap_h, full_bar(s), kc * kBlockK, row, cmask, pol_h);
+            mbar_arrive_expect_tx(full_bar(s), p.stage_bytes);
+            if (p.box3d) {
+              tma_load_3d(a, &tmap_w, full_bar(s), 0, vt * kBlockV, kc * p.kc, pol_w);
+              tma_load_3d(h, &tmap_h, full_bar(s), 0, row, kc * p.kc, pol_h);
+            } else {
+              tma_load_2d(a, &tmap_w, full_bar(s), kc * kBlockK, vt * kBlockV, pol_w);
+              tma_load_2d(h, &tmap_h, full_bar(s), kc * kBlockK, row, pol_h);
             }
           }
           issued_mask |= 1u << s;
@@ -258,69 +274,89 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      if (!ok) {
-        // Let every copy already issued land before the CTA exits.
+      if (!ok && (!kPair || rank == 0)) {
+        // Let every copy already issued land before the CTA exits (a pair's
+        // copies all complete on the leader's barriers).
         for (int t = 0; t < S; ++t)
           if (issued_mask & (1u << t)) mbar_wait_drain(full_bar(t), (issued_phase >> t) & 1u);
       }
     }
   } else if (warp == 1) {
     if (lane == 0) {
-      // ------------------------------------------------------ MMA issuer --
-      const uint32_t idesc = idesc_bf16_f32(kBlockV, p.BT);
-      int s = 0;
-      uint32_t ph = 0;
-      int ul = 0;
-      bool ok = true;
-      PieceIter itr(p);
-      Piece pc;
-      while (ok && itr.next(p, pc)) {
-        const int acc = ul & 1;
-        const uint32_t aph = (uint32_t)(ul >> 1) & 1u;
-        if (!mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.BT);
-        for (int kc = pc.kb; kc < pc.ke; ++kc) {
-          if (!mbar_wait(full_bar(s), ph, abort_flag, p.status)) {
+      if (kPair && rank == 1) {
+        // The pair's MMAs are issued by the leader; nothing to do here.
+      } else {
+        // ---------------------------------------------------- MMA issuer --
+        const uint32_t idesc = idesc_bf16_f32(pair ? 2 * kBlockV : kBlockV, p.BT);
+        const int h_slice_bytes = hid_rows * kBlockK * 2;   // this CTA's rows of one slice
+        int s = 0;
+        uint32_t ph = 0;
+        int ul = 0;
+        bool ok = true;
+        PieceIter itr(p);
+        Piece pc;
+        while (ok && itr.next(p, pc)) {
+          const int acc = ul & 1;
+          const uint32_t aph = (uint32_t)(ul >> 1) & 1u;
+          const bool empty_ok = pair ? mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)
+                                     : mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status);
+          if (!empty_ok) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t a = sbase + (uint32_t)s * p.stage_bytes;
-          const uint32_t h = a + (uint32_t)(p.kc * kStageA);
-          for (int c = 0; c < p.kc; ++c) {
-            // slice c: W rows [128 x 128 B] at a + c*16 KB, hidden [BT x 128 B]
-            const uint64_t adesc = smem_desc_sw128(a + (uint32_t)(c * kStageA));
-            const uint64_t bdesc = smem_desc_sw128(h + (uint32_t)(c * p.BT * kBlockK * 2));
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.BT);
+          for (int kc = pc.kb; kc < pc.ke; ++kc) {
+            const bool got = pair ? mbar_wait_cluster(full_bar(s), ph, abort_flag, p.status)
+                                  : mbar_wait(full_bar(s), ph, abort_flag, p.status);
+            if (!got) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a = sbase + (uint32_t)s * p.stage_bytes;
+            const uint32_t h = a + (uint32_t)(p.kc * kStageA);
+            for (int c = 0; c < p.kc; ++c) {
+              // slice c: W rows [128 x 128 B] at a + c*16 KB, token rows [BT/K x 128 B]
+              const uint64_t adesc = smem_desc_sw128(a + (uint32_t)(c * kStageA));
+              const uint64_t bdesc = smem_desc_sw128(h + (uint32_t)(c * h_slice_bytes));
 #pragma unroll
-            for (int k = 0; k < kBlockK / 16; ++k)
-              tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc,
-                          (kc > pc.kb || c > 0 || k > 0) ? 1u : 0u);
+              for (int k = 0; k < kBlockK / 16; ++k) {
+                const uint32_t accum = (kc > pc.kb || c > 0 || k > 0) ? 1u : 0u;
+                if constexpr (kPair)
+                  tc2_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accum);
+                else
+                  tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accum);
+              }
+            }
+            if constexpr (kPair)
+              tc2_commit_mc(empty_bar(s), 3);   // the stage is free in both CTAs
+            else
+              tc_commit(empty_bar(s));
+            if (++s == S) {
+              s = 0;
+              ph ^= 1u;
+            }
           }
-          if (p.K > 1)
-            tc_commit_mc(empty_bar(s), cmask);   // the stage is free in every partner too
+          if (!ok) break;
+          if constexpr (kPair)
+            tc2_commit_mc(tfull_bar(acc), 3);
           else
-            tc_commit(empty_bar(s));
-          if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-          }
+            tc_commit(tfull_bar(acc));
+          ++ul;
         }
-        if (!ok) break;
-        tc_commit(tfull_bar(acc));
-        ++ul;
+        // All MMAs this thread issued are complete once this phase ends.
+        if constexpr (kPair)
+          tc2_commit_mc(mma_done_bar, 1);
+        else
+          tc_commit(mma_done_bar);
+        mbar_wait_drain(mma_done_bar, 0);
       }
-      // All MMAs this thread issued are complete once this phase ends.
-      tc_commit(mma_done_bar);
-      mbar_wait_drain(mma_done_bar, 0);
     }
-  } else if (warp >= 6) {
+  } else if (warp >= kQWarp0) {
     // ---------------------------------------------------------- q-warps --
     if (p.ep.sample && p.ep.q_warps) {
-      const int qw = warp - 6;
+      const int qw = warp - kQWarp0;
       const int g1 = p.gamma + 1;
       const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(p.ep.dl);
       PieceIter itr(p);
@@ -375,13 +411,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (p.stream_k) {
         named_bar_sync(3, 128);
         const int n_draft = (p.M / g1) * p.gamma + min(p.M % g1, p.gamma);
-        for (int r = threadIdx.x - 192; r < n_draft; r += 128)
+        for (int r = threadIdx.x - 32 * kQWarp0; r < n_draft; r += 128)
           p.ep.pq[(size_t)r * p.ep.P + blockIdx.x] = qrun[r];
       }
     }
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;                 // TMEM lane quarter of this warp
+    const int grp = (warp - 2) >> 2;        // chunk group: pairs 2*grp, 2*grp + 4, ...
     const int epi_tid = threadIdx.x - 64;
     const int row = q * 32 + lane;          // vocabulary row within the tile
     const size_t slot_floats = (size_t)p.BT * kBlockV;
@@ -398,10 +435,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tt = pc.unit % p.n_tt;
       const int v = vt * kBlockV + row;
       const int m_base = tt * p.BT;
-      if (epi_tid == 0) *epi_flag = mbar_wait(tfull_bar(acc), aph, abort_flag, p.status) ? 1 : 0;
-      named_bar_sync(1, 128);
+      if (epi_tid == 0)
+        *epi_flag = (pair ? mbar_wait_cluster(tfull_bar(acc), aph, abort_flag, p.status)
+                          : mbar_wait(tfull_bar(acc), aph, abort_flag, p.status))
+                        ? 1
+                        : 0;
+      named_bar_sync(1, kEpiThreads);
       const bool ok = *epi_flag != 0;
-      named_bar_sync(2, 128);
+      named_bar_sync(2, kEpiThreads);
       if (!ok) break;
       tc_fence_after();
       const int n_chunks = (min(p.BT, p.M - m_base) + 15) / 16;
@@ -419,31 +460,31 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int part = pc.kb > 0 ? 1 : 0;
         float* mine = p.fix + ((size_t)slot * 2 + part) * slot_floats;
         other = p.fix + ((size_t)slot * 2 + (1 - part)) * slot_floats;
-        for (int c = 0; c < n_chunks; ++c) {
+        for (int c = grp; c < n_chunks; c += 2) {
           float accv[16];
           tmem_ld16(tbase + (uint32_t)(c * 16), accv);
 #pragma unroll
           for (int n = 0; n < 16; ++n) __stcg(mine + (size_t)(c * 16 + n) * kBlockV + row, accv[n]);
         }
         __threadfence();
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
         if (epi_tid == 0) {
           // The part that finds this call's epoch already there arrives second.
           const unsigned long long prev = atomicExch(p.fix_tickets + slot, p.epoch);
           __threadfence();
           *epi_flag = prev == p.epoch ? 1 : 0;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
         finish = *epi_flag != 0;
-        named_bar_sync(2, 128);
+        named_bar_sync(2, kEpiThreads);
         if (finish) __threadfence();
       }
       if (finish) {
         const bool vvalid = v < p.V;
         // Per 16-column chunk: logits out, then each warp's (max, sum exp2)
         // and argmax per column into red[warp quarter][column]. Two chunks
-        // per tensor-memory load.
-        for (int c = 0; c < n_chunks; c += 2) {
+        // per tensor-memory load; the two warp groups take alternate pairs.
+        for (int c = 2 * grp; c < n_chunks; c += 4) {
           float accv[32];
           const int nh = c + 1 < n_chunks ? 2 : 1;
           if (nh == 2) {
@@ -479,11 +520,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if ((lane & 1) == 0) red[q * p.BT + cc * 16 + (lane >> 1)] = r;
           }
         }
-        named_bar_sync(1, 128);
-        // Columns across the four warp quarters, 128 columns at a time;
-        // column col is always folded by thread col % 128.
+        named_bar_sync(1, kEpiThreads);
+        // Columns across the four warp quarters, 256 columns at a time;
+        // column col is always folded by thread col % 256.
         const int ncols = min(p.BT, p.M - m_base);
-        for (int col = epi_tid; col < ncols; col += 128) {
+        for (int col = epi_tid; col < ncols; col += kEpiThreads) {
           PartialP a = red[col];
 #pragma unroll
           for (int qq = 1; qq < 4; ++qq) partialp_merge(a, red[qq * p.BT + col], p.ep.c);
@@ -493,26 +534,33 @@ __global__ void __launch_bounds__(kThreads, 1)
           else
             p.ep.pp[(size_t)m * p.ep.P + vt] = a;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, kEpiThreads);
       }
       tc_fence_before();
-      mbar_arrive(tempty_bar(acc));
+      if (pair && rank == 1)
+        mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));   // the leader's MMA reuses it
+      else
+        mbar_arrive(tempty_bar(acc));
     }
     if (p.stream_k) {
       // One record per token row for everything this CTA finished.
-      named_bar_sync(1, 128);
-      for (int m = epi_tid; m < p.M; m += 128) p.ep.pp[(size_t)m * p.ep.P + blockIdx.x] = run[m];
+      named_bar_sync(1, kEpiThreads);
+      for (int m = epi_tid; m < p.M; m += kEpiThreads) p.ep.pp[(size_t)m * p.ep.P + blockIdx.x] = run[m];
     }
   }
 
   __syncthreads();
+  // A pair deallocates collectively, once both CTAs are done with it and
+  // with each other's barriers.
+  if (pair) cluster_sync_all();
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, p.tmem_cols);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, p.tmem_cols);
+    else
+      tmem_dealloc(tmem_base, p.tmem_cols);
   }
-  // Partners may still arrive on this CTA's barriers until they finish.
-  if (p.K > 1) cluster_sync_all();
 }
 
 int max_clusters_cached(int smem_bytes, int K) {
@@ -520,7 +568,7 @@ int max_clusters_cached(int smem_bytes, int K) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   if (cache[dev][0] == smem_bytes && cache[dev][1] == K) return cache[dev][2];
-  auto kern = lmhead_tc_kernel<__nv_bfloat16>;
+  auto kern = lmhead_tc_kernel<__nv_bfloat16, true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
       cudaSuccess)
     return 0;
@@ -556,7 +604,10 @@ TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters) {
   // else 1 (the stream rates these caps were chosen from are in the kernel
   // header comment).
   const int budget = kSmemLimit - 1024 - misc_bytes(g.BT);
-  const int slice_bytes = kStageA + g.BT * kBlockK * 2;
+  g.n_vt = (V + kBlockV - 1) / kBlockV;
+  g.K = (g.BT >= kClusterMinBT && g.n_vt >= 2) ? 2 : 1;
+  // A CTA holds 128 W rows and BT/K token rows of every slice.
+  const int slice_bytes = kStageA + (g.BT / g.K) * kBlockK * 2;
   g.box3d = d % kBlockK == 0 ? 1 : 0;
   if (g.box3d && budget / (4 * slice_bytes) >= 3) {
     g.kc = 4;
@@ -574,8 +625,6 @@ TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters) {
   while (cols < 2 * g.BT) cols <<= 1;
   g.tmem_cols = cols;
   g.smem_bytes = 1024 + g.stages * g.stage_bytes + misc_bytes(g.BT);
-  g.n_vt = (V + kBlockV - 1) / kBlockV;
-  g.K = (g.BT >= kClusterMinBT && g.n_vt >= 2) ? 2 : 1;
   g.n_units = ((g.n_vt + g.K - 1) / g.K) * g.n_tt;
   g.nk = ((d + kBlockK - 1) / kBlockK + g.kc - 1) / g.kc;
   const int sms = num_sms < kMaxGrid ? num_sms : kMaxGrid;
@@ -625,16 +674,18 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   p.ep.run = nullptr;
   p.ep.q_in_epilogue = 0;   // q-warps (ep.q_warps) or the standalone stream reduce q
   // The tensor-core path exists for bf16 inputs; draft logits share the dtype.
-  auto kern = lmhead_tc_kernel<__nv_bfloat16>;
-  // The shared-memory opt-in is set once per device and size.
-  static int smem_set[kMaxDevices] = {0};
+  auto kern = g.K > 1 ? lmhead_tc_kernel<__nv_bfloat16, true>
+                      : lmhead_tc_kernel<__nv_bfloat16, false>;
+  // The shared-memory opt-in is set once per device, build and size.
+  static int smem_set[kMaxDevices][2] = {{0}};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  if (dev < 0 || dev >= kMaxDevices || smem_set[dev] != g.smem_bytes) {
+  const int which = g.K > 1 ? 1 : 0;
+  if (dev < 0 || dev >= kMaxDevices || smem_set[dev][which] != g.smem_bytes) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
     if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < kMaxDevices) smem_set[dev] = g.smem_bytes;
+    if (dev >= 0 && dev < kMaxDevices) smem_set[dev][which] = g.smem_bytes;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.grid);

@@ -64,6 +64,7 @@ cudaError_t launch_accept(const AcceptLaunch& L, cudaStream_t stream);
 // Residual / bonus draw for every sequence (sampling mode).
 struct SampleLaunch {
   int B, gamma, V, nchunks, dl_bf16;
+  int vec;          // set by the launcher: 16-byte logit and draft-logit loads are aligned
   float c;
   uint64_t seed;
   const float* z;

@@ -8,50 +8,127 @@
 //
 // The draw inverts the prefix sum C of the weights w in token-ID order at
 // t = u * S (S the total): the token is the smallest v with C_v > t. Grid =
-// (V chunks of 4096, B). Each CTA sums its chunk's weights; the last CTA of
-// a sequence to finish (atomic ticket, no waiting) scans the chunk sums in
-// order, finds the chunk holding t, rescans that chunk and writes the token.
+// (V chunks of 4096, B). Each CTA sums its chunk's weights, reading the
+// chunk as four coalesced 1024-token sweeps (16-byte logit loads, 8-byte
+// draft-logit loads, all issued before the arithmetic). The last CTA of a
+// sequence to finish (atomic ticket, no waiting) forms the prefix of the
+// chunk sums with one warp, finds the chunk holding t, rescans that chunk in
+// token order (16 contiguous tokens per thread) and writes the token.
 #include "kernels.h"
 
 namespace specdec {
 namespace {
 
-constexpr int kPer = kChunkV / kSampleThreads;   // 16 tokens per thread
+constexpr int kVec = 4;                              // tokens per load
+constexpr int kSweep = kSampleThreads * kVec;        // 1024 tokens per sweep
+constexpr int kSweeps = kChunkV / kSweep;            // 4 sweeps per chunk
+constexpr int kPer = kChunkV / kSampleThreads;       // 16 tokens per thread
 constexpr int kMaxChunks = kMaxVocab / kChunkV;
+static_assert(kSweeps * kVec == kPer, "chunk layout");
 
+struct Raw4 {
+  float4 z;
+  float q[kVec];
+};
+
+// Logits and draft logits of tokens v .. v+3 (v a multiple of 4); tokens at
+// or past V read as weight-free (-inf logit for p, nothing for q).
 template <typename DL>
-__device__ __forceinline__ void chunk_weights(const float* __restrict__ zr,
-                                              const DL* __restrict__ qr, const SelectedRow& sr,
-                                              bool residual, float c, int V, int v0,
-                                              float (&w)[kPer]) {
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int v = v0 + k;
-    float x = 0.f;
-    if (v < V) {
-      const float p = exp2f((zr[v] - sr.mp) * c - sr.lsp);
-      if (residual) {
-        const float qv = exp2f((load_logit(qr, (size_t)v) - sr.mq) * c - sr.lsq);
-        x = fmaxf(0.f, p - qv);
+__device__ __forceinline__ Raw4 load4(const float* __restrict__ zr, const DL* __restrict__ qr,
+                                      int v, int V, bool vec, bool residual) {
+  Raw4 r;
+  if (vec && v < V) {   // V % 4 == 0: the whole group is in range
+    r.z = __ldg(reinterpret_cast<const float4*>(zr + v));
+    if (residual) {
+      if constexpr (sizeof(DL) == 2) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(qr + v));
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+        r.q[0] = a.x; r.q[1] = a.y; r.q[2] = b.x; r.q[3] = b.y;
       } else {
-        x = p;
+        const float4 f = __ldg(reinterpret_cast<const float4*>(qr + v));
+        r.q[0] = f.x; r.q[1] = f.y; r.q[2] = f.z; r.q[3] = f.w;
       }
     }
-    w[k] = x;
+    return r;
+  }
+  float zz[kVec];
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) {
+    const bool in = v + e < V;
+    zz[e] = in ? zr[v + e] : -INFINITY;
+    r.q[e] = (in && residual) ? load_logit(qr, (size_t)(v + e)) : 0.f;
+  }
+  r.z = make_float4(zz[0], zz[1], zz[2], zz[3]);
+  return r;
+}
+
+// w = max(0, p - q) (residual) or p, for the four tokens of a group.
+__device__ __forceinline__ void weights4(const Raw4& r, const SelectedRow& sr, bool residual,
+                                         float c, float* w) {
+  const float zz[kVec] = {r.z.x, r.z.y, r.z.z, r.z.w};
+#pragma unroll
+  for (int e = 0; e < kVec; ++e) {
+    const float p = exp2f((zz[e] - sr.mp) * c - sr.lsp);
+    if (residual) {
+      const float qv = exp2f((r.q[e] - sr.mq) * c - sr.lsq);
+      w[e] = fmaxf(0.f, p - qv);
+    } else {
+      w[e] = p;
+    }
   }
 }
 
-// Block sum in a fixed order: per-thread sequential, then warp shuffles,
-// then the 8 warp sums in order.
-__device__ __forceinline__ float block_sum(float x, float* red) {
-  x = warp_sum(x);
+// Sum of one chunk's weights: four coalesced sweeps, thread-sequential,
+// then warp shuffles, then the 8 warp sums in order. Every thread returns
+// the chunk total.
+template <typename DL>
+__device__ __forceinline__ float chunk_total(const float* zr, const DL* qr, const SelectedRow& sr,
+                                             bool residual, float c, int V, bool vec, int chunk,
+                                             float* red) {
+  const int v0 = chunk * kChunkV + threadIdx.x * kVec;
+  Raw4 raw[kSweeps];
+#pragma unroll
+  for (int k = 0; k < kSweeps; ++k) raw[k] = load4<DL>(zr, qr, v0 + k * kSweep, V, vec, residual);
+  float ts = 0.f;
+#pragma unroll
+  for (int k = 0; k < kSweeps; ++k) {
+    float w[kVec];
+    weights4(raw[k], sr, residual, c, w);
+#pragma unroll
+    for (int e = 0; e < kVec; ++e) ts += w[e];
+  }
+  ts = warp_sum(ts);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
-  if (lane == 0) red[warp] = x;
+  if (lane == 0) red[warp] = ts;
   __syncthreads();
   float t = 0.f;
   for (int i = 0; i < kSampleThreads / 32; ++i) t += red[i];
   return t;
+}
+
+// Warp 0: inclusive prefix of the chunk sums in chunk order (groups of 32,
+// shuffle scan, carried total), and the last chunk holding weight.
+__device__ __forceinline__ void prefix_chunks(const float* cs, float* pre, int n, int* last_pos) {
+  const int lane = threadIdx.x & 31;
+  float carry = 0.f;
+  int lp = -1;
+  for (int g = 0; g < n; g += 32) {
+    const int k = g + lane;
+    const float x = k < n ? cs[k] : 0.f;
+    float incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (k < n) pre[k] = carry + incl;
+    const unsigned pos = __ballot_sync(0xffffffffu, k < n && x > 0.f);
+    if (pos) lp = g + 31 - __clz(pos);
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) *last_pos = lp;
 }
 
 template <typename DL>
@@ -59,9 +136,11 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   __shared__ float red[kSampleThreads / 32];
   __shared__ float wscan[kSampleThreads / 32];
   __shared__ float s_cs[kMaxChunks];
+  __shared__ float s_pre[kMaxChunks];
   __shared__ int s_last;
   __shared__ int s_tok;
   __shared__ int s_lastpos;
+  __shared__ int s_lastchunk;
   __shared__ int s_chunk;
   __shared__ float s_before, s_t;
   __shared__ int s_residual;
@@ -75,14 +154,11 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   const float* zr = L.z + (size_t)(b * g1 + sr.j) * L.V;
   const DL* qr = sr.residual ? static_cast<const DL*>(L.dl) + ((size_t)b * L.gamma + sr.j) * L.V
                              : nullptr;
+  const bool vec = L.vec != 0;
   const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
 
-  float w[kPer];
-  chunk_weights<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, chunk * kChunkV + tid * kPer, w);
-  float ts = 0.f;
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) ts += w[k];
-  const float total = block_sum(ts, red);
+  const float total = chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, vec, chunk, red);
   if (tid == 0) {
     L.chunk_sums[(size_t)b * L.nchunks + chunk] = total;
     __threadfence();
@@ -98,66 +174,52 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   for (int k = tid; k < L.nchunks; k += kSampleThreads)
     s_cs[k] = __ldcg(L.chunk_sums + (size_t)b * L.nchunks + k);
   __syncthreads();
-  if (tid == 0) {
-    float S = 0.f;
-    for (int k = 0; k < L.nchunks; ++k) S += s_cs[k];
-    s_residual = sr.residual;
-    if (sr.residual && !(S > 0.f)) s_residual = 0;   // p == q to rounding: draw from p
-    s_t = u * S;
-  }
+  if (warp == 0) prefix_chunks(s_cs, s_pre, L.nchunks, &s_lastchunk);
   __syncthreads();
-  if (s_residual != sr.residual) {
-    // Fallback: recompute every chunk sum with w = p.
+  bool residual = sr.residual != 0;
+  if (residual && !(s_pre[L.nchunks - 1] > 0.f)) {
+    // p == q to rounding: draw from p. Recompute every chunk sum with w = p.
+    residual = false;
     for (int k = 0; k < L.nchunks; ++k) {
-      float wk[kPer];
-      chunk_weights<DL>(zr, qr, sr, false, L.c, L.V, k * kChunkV + tid * kPer, wk);
-      float t2 = 0.f;
-#pragma unroll
-      for (int e = 0; e < kPer; ++e) t2 += wk[e];
-      const float tot = block_sum(t2, red);
+      const float tot = chunk_total<DL>(zr, qr, sr, false, L.c, L.V, vec, k, red);
       if (tid == 0) s_cs[k] = tot;
     }
     __syncthreads();
-    if (tid == 0) {
-      float S = 0.f;
-      for (int k = 0; k < L.nchunks; ++k) S += s_cs[k];
-      s_t = u * S;
-    }
+    if (warp == 0) prefix_chunks(s_cs, s_pre, L.nchunks, &s_lastchunk);
     __syncthreads();
   }
-  if (tid == 0) {
-    const float* cs = s_cs;
-    const float t = s_t;
-    float acc = 0.f;
-    int found = -1, last_pos = 0;
-    float before = 0.f;
-    for (int k = 0; k < L.nchunks; ++k) {
-      const float nxt = acc + cs[k];
-      if (cs[k] > 0.f) last_pos = k;
-      if (found < 0 && nxt > t) {
-        found = k;
-        before = acc;
-      }
-      acc = nxt;
+  if (warp == 0) {
+    const float t = u * s_pre[L.nchunks - 1];
+    int found = -1;
+    for (int g = 0; g < L.nchunks && found < 0; g += 32) {
+      const int k = g + lane;
+      const unsigned hit = __ballot_sync(0xffffffffu, k < L.nchunks && s_pre[k] > t);
+      if (hit) found = g + __ffs(hit) - 1;
     }
-    if (found < 0) {   // t rounded up to S: the last chunk with weight
-      found = last_pos;
-      before = acc - cs[last_pos];
+    if (found < 0) found = s_lastchunk;   // t rounded up to S: the last chunk with weight
+    if (found < 0) found = 0;             // no weight at all (cannot happen for w = p)
+    if (lane == 0) {
+      s_chunk = found;
+      s_before = found > 0 ? s_pre[found - 1] : 0.f;
+      s_t = t;
+      s_tok = 0x7fffffff;
+      s_lastpos = -1;
+      s_residual = residual;
     }
-    s_chunk = found;
-    s_before = before;
-    s_tok = 0x7fffffff;
-    s_lastpos = -1;
   }
   __syncthreads();
 
-  // ---- rescan the chosen chunk in token order ----
+  // ---- rescan the chosen chunk in token order: 16 contiguous tokens per thread ----
   const int v0 = s_chunk * kChunkV + tid * kPer;
-  chunk_weights<DL>(zr, qr, sr, s_residual != 0, L.c, L.V, v0, w);
-  ts = 0.f;
+  float w[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer / kVec; ++k) {
+    const Raw4 r = load4<DL>(zr, qr, v0 + k * kVec, L.V, vec, s_residual != 0);
+    weights4(r, sr, s_residual != 0, L.c, w + k * kVec);
+  }
+  float ts = 0.f;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) ts += w[k];
-  const int warp = tid >> 5, lane = tid & 31;
   float incl = ts;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -191,7 +253,13 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
 
 }  // namespace
 
-cudaError_t launch_sample(const SampleLaunch& L, cudaStream_t stream) {
+cudaError_t launch_sample(const SampleLaunch& L0, cudaStream_t stream) {
+  SampleLaunch L = L0;
+  const uintptr_t dl_align = L.dl_bf16 ? 8 : 16;
+  L.vec = (L.V % kVec == 0 && ((uintptr_t)L.z & 15u) == 0 &&
+           ((uintptr_t)L.dl & (dl_align - 1)) == 0)
+              ? 1
+              : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.nchunks, L.B);
   cfg.blockDim = dim3(kSampleThreads);

@@ -112,6 +112,21 @@ bool encode_bf16_rows(CUtensorMap* map, const void* base, int rows, int cols, in
 // one load brings box_slices adjacent 128-byte pieces of every row, stored
 // slice-major as box_slices standard [box_rows x 128 B] swizzled tiles.
 // Needs cols % 64 == 0.
+// fp32 logits [rows, cols] as 32 x 32 tiles in the 128-byte swizzled layout
+// (the row-owner epilogue's bulk stores). Needs cols % 4 == 0 and a 16-byte
+// aligned base.
+bool encode_f32_tiles(CUtensorMap* map, void* base, int rows, int cols) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool encode_bf16_rows3d(CUtensorMap* map, const void* base, int rows, int cols, int box_rows,
                         int box_slices) {
   auto fn = encode_fn();
@@ -213,9 +228,13 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
                             : (encode_bf16_rows(&tw, W, V, d, kBlockV) &&
                                encode_bf16_rows(&th, hidden, pl.M, d, h_rows));
     if (!ok) return SPECDEC_ERR_CUDA;
+    CUtensorMap tz;
+    const bool ztma = g.rowown && z != nullptr && V % 4 == 0 && ((uintptr_t)z & 15u) == 0 &&
+                      encode_f32_tiles(&tz, z, pl.M, V);
     TcLaunch L;
     L.tmap_w = &tw;
     L.tmap_h = &th;
+    L.tmap_z = ztma ? &tz : nullptr;
     L.M = pl.M;
     L.V = V;
     L.d = d;
@@ -443,6 +462,7 @@ int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void*
   TcLaunch L;
   L.tmap_w = &tw;
   L.tmap_h = &th;
+  L.tmap_z = nullptr;
   L.M = pl.M;
   L.V = V;
   L.d = d;

@@ -357,6 +357,26 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
       : "memory");
 }
 // Each thread of the warp reads 16 consecutive fp32 columns of its lane.
+// Bulk tensor store (shared -> global) and its completion groups.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t smem, int x, int y) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
+      "r"(smem), "r"(x), "r"(y)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, float a, float b, float c, float d) {
+  asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
   uint32_t r[16];
   asm volatile(
@@ -536,6 +556,58 @@ __device__ __forceinline__ void warp_argmax16(const float (&x)[16], int idx, flo
     v[0] = rv;
     i[0] = ri;
   }
+  v_out = v[0];
+  i_out = i[0];
+}
+
+// 32-column forms of the two reductions above, for one 32-column tensor
+// memory load: five halving exchanges (xor 16, 8, 4, 2, 1) leave lane L
+// holding column L, merged over all 32 rows exactly once (no duplicate
+// pair). Twice the independent chains of the 16-column form at each level.
+__device__ __forceinline__ void warp_softmax32(const float (&x)[32], float c, float& m_out,
+                                               float& s_out) {
+  const int lane = threadIdx.x & 31;
+  float m[16], s[16];
+  const bool upper = (lane & 16) != 0;
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float keep = upper ? x[16 + k] : x[k];
+    const float send = upper ? x[k] : x[16 + k];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    const float mm = fmaxf(keep, recv);
+    m[k] = mm;
+    s[k] = mm == -INFINITY ? 0.f : 1.f + exp2f(-fabsf(keep - recv) * c);
+  }
+  osm_halve<8>(m, s, (lane & 8) != 0, 8, c);
+  osm_halve<4>(m, s, (lane & 4) != 0, 4, c);
+  osm_halve<2>(m, s, (lane & 2) != 0, 2, c);
+  osm_halve<1>(m, s, (lane & 1) != 0, 1, c);
+  m_out = m[0];
+  s_out = s[0];
+}
+__device__ __forceinline__ void warp_argmax32(const float (&x)[32], int idx, float& v_out,
+                                              int& i_out) {
+  const int lane = threadIdx.x & 31;
+  float v[16];
+  int i[16];
+  const bool upper = (lane & 16) != 0;
+  const int ridx = __shfl_xor_sync(0xffffffffu, idx, 16);
+#pragma unroll
+  for (int k = 0; k < 16; ++k) {
+    const float keep = upper ? x[16 + k] : x[k];
+    const float send = upper ? x[k] : x[16 + k];
+    const float recv = __shfl_xor_sync(0xffffffffu, send, 16);
+    v[k] = keep;
+    i[k] = idx;
+    if (argmax_better(recv, ridx, v[k], i[k])) {
+      v[k] = recv;
+      i[k] = ridx;
+    }
+  }
+  amax_halve<8>(v, i, (lane & 8) != 0, 8);
+  amax_halve<4>(v, i, (lane & 4) != 0, 4);
+  amax_halve<2>(v, i, (lane & 2) != 0, 2);
+  amax_halve<1>(v, i, (lane & 1) != 0, 1);
   v_out = v[0];
   i_out = i[0];
 }

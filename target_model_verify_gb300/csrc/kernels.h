@@ -15,6 +15,7 @@ namespace specdec {
 struct TcLaunch {
   const CUtensorMap* tmap_w;     // W_lm [V, d], box {64, 128}, 128B swizzle
   const CUtensorMap* tmap_h;     // hidden [M, d], box {64, BT}, 128B swizzle
+  const CUtensorMap* tmap_z;     // logits [M, V] fp32, box {32, 32}, 128B swizzle; or null
   int M, V, d, gamma;
   int* status;
   float* fix;                    // stream-K fix-up slots (tc_fix_floats floats)
@@ -94,6 +95,7 @@ struct TcGeometry {
   int n_units, nk, grid;
   int stream_k;                  // one token tile: contiguous k-iteration ranges
   int records;                   // partial records per row (grid or vocabulary tiles)
+  int rowown;                    // 1: tokens on the MMA's M side (pairs, 256-row token tiles)
 };
 TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters);
 // Co-resident clusters of the kernel for this shape on the current device

@@ -82,6 +82,11 @@ __host__ __device__ constexpr int misc_bytes(int BT) {
 }
 constexpr int kMaxDevices = 64;
 constexpr int kClusterMinBT = 64;  // token tiles from this size share hidden slices
+// Row-owner logit staging: one 32 x 32 fp32 tile (4 KB) per epilogue warp,
+// written in the 128-byte swizzled layout the bulk tensor store reads.
+constexpr int kZStageBytes = 4096;
+constexpr int kZStaging = 8 * kZStageBytes;
+__host__ __device__ constexpr int misc_span(int BT) { return (misc_bytes(BT) + 1023) & ~1023; }
 
 struct TcParams {
   int M, V, d, gamma;
@@ -99,6 +104,7 @@ struct TcParams {
   unsigned long long* fix_tickets;   // [slots]: epoch of the last part to arrive
   unsigned long long epoch;      // this call's tag (never repeats within a process)
   int withhold_loads;            // self-test: issue no loads, so the first wait runs out
+  int z_tma;                     // row owner: logits leave through bulk tensor stores
   EpiParams ep;
 };
 
@@ -151,11 +157,14 @@ __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
 }
 
 // kPair: the 2-SM (CTA pair) build; cta_group::1 and ::2 instructions cannot
-// share a kernel.
-template <typename DL, bool kPair>
+// share a kernel. kRowOwn (pairs with 256-row token tiles): tokens on the
+// MMA's M side, so tensor-memory lane = token row and each epilogue thread
+// owns one token row.
+template <typename DL, bool kPair, bool kRowOwn>
 __global__ void __launch_bounds__(kThreads, 1)
     lmhead_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                     const __grid_constant__ CUtensorMap tmap_h, const TcParams p) {
+                     const __grid_constant__ CUtensorMap tmap_h,
+                     const __grid_constant__ CUtensorMap tmap_z, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;
@@ -323,7 +332,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
               for (int k = 0; k < kBlockK / 16; ++k) {
                 const uint32_t accum = (kc > pc.kb || c > 0 || k > 0) ? 1u : 0u;
-                if constexpr (kPair)
+                if constexpr (kRowOwn)   // A = token rows, B = W rows
+                  tc2_mma_bf16(d_tmem, bdesc + 2u * k, adesc + 2u * k, idesc, accum);
+                else if constexpr (kPair)
                   tc2_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accum);
                 else
                   tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accum);
@@ -415,6 +426,171 @@ __global__ void __launch_bounds__(kThreads, 1)
           p.ep.pq[(size_t)r * p.ep.P + blockIdx.x] = qrun[r];
       }
     }
+  } else if constexpr (kRowOwn) {
+    // ------------------------------------------------ epilogue, row owner --
+    // Tensor-memory lane = token row: thread (quarter q, lane) owns token
+    // row r = 32q + lane of this CTA's 128 and reduces its softmax and
+    // argmax partials in registers, 32 vocabulary columns per load; the two
+    // warp groups take alternate chunks and merge once per record.
+    const int q = warp & 3;
+    const int grp = (warp - 2) >> 2;
+    const int r = q * 32 + lane;
+    const size_t slot_floats = (size_t)p.BT * kBlockV;
+    const bool vsample = p.ep.sample != 0;
+    const bool vargmax = p.ep.want_argmax != 0;
+    const bool zvec = (p.V & 3) == 0 && ((uintptr_t)p.ep.zout & 15u) == 0;
+    const bool ztma = p.z_tma != 0 && p.ep.zout != nullptr;
+    const uint32_t zstg = sbase + (uint32_t)(S * p.stage_bytes + misc_span(p.BT)) +
+                          (uint32_t)((warp - 2) * kZStageBytes);
+    const int n32 = p.BT / 32;               // 32-column chunks of the 256-wide vocabulary tile
+    PartialP st{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+    int m = rank * 128 + r;                  // token row (stream-K: the only token tile)
+    int ul = 0;
+    PieceIter itr(p);
+    Piece pc;
+    while (itr.next(p, pc)) {
+      const int acc = ul & 1;
+      const uint32_t aph = (uint32_t)(ul >> 1) & 1u;
+      ++ul;
+      const int vt2 = pc.unit / p.n_tt;      // vocabulary tile of 256 (both CTAs' W rows)
+      const int tt = pc.unit % p.n_tt;
+      m = tt * p.BT + rank * 128 + r;
+      if (threadIdx.x == 64)
+        *epi_flag = (mbar_wait_cluster(tfull_bar(acc), aph, abort_flag, p.status)) ? 1 : 0;
+      named_bar_sync(1, kEpiThreads);
+      const bool ok = *epi_flag != 0;
+      named_bar_sync(2, kEpiThreads);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.BT);
+      bool finish = true;
+      const float* other = nullptr;
+      if (pc.kb > 0 || pc.ke < p.nk) {
+        // Tile shared with the neighbouring cluster (see the swap-AB path).
+        const int bnd = pc.kb > 0 ? cid : cid + 1;
+        const int slot = bnd * p.K + rank;
+        const int part = pc.kb > 0 ? 1 : 0;
+        float* mine = p.fix + ((size_t)slot * 2 + part) * slot_floats;
+        other = p.fix + ((size_t)slot * 2 + (1 - part)) * slot_floats;
+        for (int c = grp; c < n32; c += 2) {
+          float accv[32];
+          tmem_ld32(tbase + (uint32_t)(c * 32), accv);
+#pragma unroll
+          for (int n = 0; n < 32; ++n) __stcg(mine + (size_t)(c * 32 + n) * kBlockV + r, accv[n]);
+        }
+        __threadfence();
+        named_bar_sync(1, kEpiThreads);
+        if (threadIdx.x == 64) {
+          const unsigned long long prev = atomicExch(p.fix_tickets + slot, p.epoch);
+          __threadfence();
+          *epi_flag = prev == p.epoch ? 1 : 0;
+        }
+        named_bar_sync(1, kEpiThreads);
+        finish = *epi_flag != 0;
+        named_bar_sync(2, kEpiThreads);
+        if (finish) __threadfence();
+      }
+      const bool mvalid = m < p.M;
+      if (finish) {
+        for (int c = grp; c < n32; c += 2) {
+          float z[32];
+          tmem_ld32(tbase + (uint32_t)(c * 32), z);
+          if (other != nullptr) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n) z[n] += __ldcg(other + (size_t)(c * 32 + n) * kBlockV + r);
+          }
+          const int v0 = vt2 * p.BT + c * 32;
+          const bool full = v0 + 32 <= p.V;
+          const int mw = m - lane;                 // the warp's first token row
+          if (ztma) {
+            // Through shared memory: this lane's row, 16-byte units swizzled
+            // by row, then one bulk tensor store of the warp's 32 x 32 tile
+            // (rows past M and columns past V are clipped by the copy).
+            if (mw < p.M && v0 < p.V) {
+              if (lane == 0) bulk_wait_read0();    // the previous tile has left the buffer
+              __syncwarp();
+              const uint32_t rowa = zstg + (uint32_t)(lane * 128);
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                st_shared_v4(rowa + (uint32_t)(((k ^ (lane & 7)) & 7) << 4), z[4 * k], z[4 * k + 1],
+                             z[4 * k + 2], z[4 * k + 3]);
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmap_z, zstg, v0, mw);
+                bulk_commit();
+              }
+            }
+          } else if (p.ep.zout != nullptr && mvalid) {
+            float* zr = p.ep.zout + (size_t)m * p.V + v0;
+            if (full && zvec) {
+#pragma unroll
+              for (int k = 0; k < 8; ++k)
+                __stcs(reinterpret_cast<float4*>(zr) + k,
+                       make_float4(z[4 * k], z[4 * k + 1], z[4 * k + 2], z[4 * k + 3]));
+            } else {
+#pragma unroll
+              for (int n = 0; n < 32; ++n)
+                if (v0 + n < p.V) __stcs(zr + n, z[n]);
+            }
+          }
+          if (!full) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n)
+              if (v0 + n >= p.V) z[n] = -INFINITY;
+          }
+          if (vsample) {
+            float mx = z[0];
+#pragma unroll
+            for (int n = 1; n < 32; ++n) mx = fmaxf(mx, z[n]);
+            const float mm = fmaxf(st.m, mx);
+            if (mm != -INFINITY) {
+              float sum = st.m == -INFINITY ? 0.f : st.s * exp2f((st.m - mm) * p.ep.c);
+#pragma unroll
+              for (int n = 0; n < 32; ++n) sum += exp2f((z[n] - mm) * p.ep.c);
+              st.m = mm;
+              st.s = sum;
+            }
+          }
+          if (vargmax) {
+#pragma unroll
+            for (int n = 0; n < 32; ++n)
+              if (z[n] > st.amax_v) {   // ascending v: strict > keeps the lowest index
+                st.amax_v = z[n];
+                st.amax_i = v0 + n;
+              }
+          }
+        }
+      }
+      tc_fence_before();
+      if (rank == 1)
+        mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+      else
+        mbar_arrive(tempty_bar(acc));
+      if (!p.stream_k) {
+        // One record per (token row, vocabulary tile): merge the two groups.
+        if (grp == 1) red[r] = st;
+        named_bar_sync(1, kEpiThreads);
+        if (grp == 0 && mvalid) {
+          PartialP a = st;
+          partialp_merge(a, red[r], p.ep.c);
+          p.ep.pp[(size_t)m * p.ep.P + vt2] = a;
+        }
+        named_bar_sync(1, kEpiThreads);
+        st = PartialP{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+      }
+    }
+    if (ztma && lane == 0) bulk_wait0();   // every logit tile is written before the CTA ends
+    if (p.stream_k) {
+      // One record per token row and cluster for everything it finished.
+      if (grp == 1) red[r] = st;
+      named_bar_sync(1, kEpiThreads);
+      if (grp == 0 && m < p.M) {
+        PartialP a = st;
+        partialp_merge(a, red[r], p.ep.c);
+        p.ep.pp[(size_t)m * p.ep.P + cid] = a;
+      }
+    }
   } else {
     // ---------------------------------------------------------- epilogue --
     const int q = warp & 3;                 // TMEM lane quarter of this warp
@@ -481,44 +657,51 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (finish) {
         const bool vvalid = v < p.V;
-        // Per 16-column chunk: logits out, then each warp's (max, sum exp2)
-        // and argmax per column into red[warp quarter][column]. Two chunks
-        // per tensor-memory load; the two warp groups take alternate pairs.
-        for (int c = 2 * grp; c < n_chunks; c += 4) {
-          float accv[32];
-          const int nh = c + 1 < n_chunks ? 2 : 1;
-          if (nh == 2) {
-            tmem_ld32(tbase + (uint32_t)(c * 16), accv);
-          } else {
-            float a16[16];
-            tmem_ld16(tbase + (uint32_t)(c * 16), a16);
+        // Per 32-column chunk (one tensor-memory load): logits out, then each
+        // warp's (max, sum exp2) and argmax per column into red[warp
+        // quarter][column], lane L holding column L. The two warp groups take
+        // alternate chunks; a 16-column tail goes to the group next in turn.
+        const int n32 = n_chunks >> 1;
+        for (int c = grp; c < n32; c += 2) {
+          float z[32];
+          tmem_ld32(tbase + (uint32_t)(c * 32), z);
+          if (other != nullptr) {
 #pragma unroll
-            for (int n = 0; n < 16; ++n) accv[n] = a16[n];
+            for (int n = 0; n < 32; ++n) z[n] += __ldcg(other + (size_t)(c * 32 + n) * kBlockV + row);
           }
-          for (int h = 0; h < nh; ++h) {
-            const int cc = c + h;
-            float z[16];
+          const int m0 = m_base + c * 32;
+          if (p.ep.zout != nullptr && vvalid) {
 #pragma unroll
-            for (int n = 0; n < 16; ++n) z[n] = accv[h * 16 + n];
-            if (other != nullptr) {
-#pragma unroll
-              for (int n = 0; n < 16; ++n)
-                z[n] += __ldcg(other + (size_t)(cc * 16 + n) * kBlockV + row);
-            }
-            const int m0 = m_base + cc * 16;
-            if (p.ep.zout != nullptr && vvalid) {
-#pragma unroll
-              for (int n = 0; n < 16; ++n)
-                if (m0 + n < p.M) __stcs(p.ep.zout + (size_t)(m0 + n) * p.V + v, z[n]);
-            }
-            float zm[16];
-#pragma unroll
-            for (int n = 0; n < 16; ++n) zm[n] = vvalid ? z[n] : -INFINITY;
-            PartialP r{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
-            if (vsample) warp_softmax16(zm, p.ep.c, r.m, r.s);
-            if (vargmax) warp_argmax16(zm, vvalid ? v : 0x7fffffff, r.amax_v, r.amax_i);
-            if ((lane & 1) == 0) red[q * p.BT + cc * 16 + (lane >> 1)] = r;
+            for (int n = 0; n < 32; ++n)
+              if (m0 + n < p.M) __stcs(p.ep.zout + (size_t)(m0 + n) * p.V + v, z[n]);
           }
+#pragma unroll
+          for (int n = 0; n < 32; ++n) z[n] = vvalid ? z[n] : -INFINITY;
+          PartialP r{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+          if (vsample) warp_softmax32(z, p.ep.c, r.m, r.s);
+          if (vargmax) warp_argmax32(z, vvalid ? v : 0x7fffffff, r.amax_v, r.amax_i);
+          red[q * p.BT + c * 32 + lane] = r;
+        }
+        if ((n_chunks & 1) && grp == (n32 & 1)) {
+          const int cc = n_chunks - 1;
+          float z[16];
+          tmem_ld16(tbase + (uint32_t)(cc * 16), z);
+          if (other != nullptr) {
+#pragma unroll
+            for (int n = 0; n < 16; ++n) z[n] += __ldcg(other + (size_t)(cc * 16 + n) * kBlockV + row);
+          }
+          const int m0 = m_base + cc * 16;
+          if (p.ep.zout != nullptr && vvalid) {
+#pragma unroll
+            for (int n = 0; n < 16; ++n)
+              if (m0 + n < p.M) __stcs(p.ep.zout + (size_t)(m0 + n) * p.V + v, z[n]);
+          }
+#pragma unroll
+          for (int n = 0; n < 16; ++n) z[n] = vvalid ? z[n] : -INFINITY;
+          PartialP r{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+          if (vsample) warp_softmax16(z, p.ep.c, r.m, r.s);
+          if (vargmax) warp_argmax16(z, vvalid ? v : 0x7fffffff, r.amax_v, r.amax_i);
+          if ((lane & 1) == 0) red[q * p.BT + cc * 16 + (lane >> 1)] = r;
         }
         named_bar_sync(1, kEpiThreads);
         // Columns across the four warp quarters, 256 columns at a time;
@@ -568,7 +751,7 @@ int max_clusters_cached(int smem_bytes, int K) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 0;
   if (cache[dev][0] == smem_bytes && cache[dev][1] == K) return cache[dev][2];
-  auto kern = lmhead_tc_kernel<__nv_bfloat16, true>;
+  auto kern = lmhead_tc_kernel<__nv_bfloat16, true, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes) !=
       cudaSuccess)
     return 0;
@@ -603,9 +786,13 @@ TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters) {
   // Slices per stage: 4 while three such stages fit, else 2 while four fit,
   // else 1 (the stream rates these caps were chosen from are in the kernel
   // header comment).
-  const int budget = kSmemLimit - 1024 - misc_bytes(g.BT);
   g.n_vt = (V + kBlockV - 1) / kBlockV;
   g.K = (g.BT >= kClusterMinBT && g.n_vt >= 2) ? 2 : 1;
+  // Token tiles of 256 on a CTA pair put the tokens on the MMA's M side
+  // (row-owner epilogue, with its logit staging).
+  g.rowown = (g.K == 2 && g.BT == 2 * kBlockV) ? 1 : 0;
+  const int misc_total = g.rowown ? misc_span(g.BT) + kZStaging : misc_bytes(g.BT);
+  const int budget = kSmemLimit - 1024 - misc_total;
   // A CTA holds 128 W rows and BT/K token rows of every slice.
   const int slice_bytes = kStageA + (g.BT / g.K) * kBlockK * 2;
   g.box3d = d % kBlockK == 0 ? 1 : 0;
@@ -624,7 +811,7 @@ TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters) {
   int cols = 32;
   while (cols < 2 * g.BT) cols <<= 1;
   g.tmem_cols = cols;
-  g.smem_bytes = 1024 + g.stages * g.stage_bytes + misc_bytes(g.BT);
+  g.smem_bytes = 1024 + g.stages * g.stage_bytes + misc_total;
   g.n_units = ((g.n_vt + g.K - 1) / g.K) * g.n_tt;
   g.nk = ((d + kBlockK - 1) / kBlockK + g.kc - 1) / g.kc;
   const int sms = num_sms < kMaxGrid ? num_sms : kMaxGrid;
@@ -634,7 +821,12 @@ TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters) {
   if (clusters < 1) clusters = 1;
   g.grid = clusters * g.K;
   g.stream_k = g.n_tt == 1 ? 1 : 0;
-  g.records = g.stream_k ? g.grid : g.n_vt;
+  // Row owner: one record per token row and cluster (stream-K) or per
+  // 256-row vocabulary tile.
+  if (g.rowown)
+    g.records = g.stream_k ? g.grid / g.K : (g.n_vt + 1) / 2;
+  else
+    g.records = g.stream_k ? g.grid : g.n_vt;
   return g;
 }
 
@@ -669,19 +861,21 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   p.fix_tickets = L.fix_tickets;
   p.epoch = L.epoch;
   p.withhold_loads = L.withhold_loads;
+  p.z_tma = (g.rowown && L.tmap_z != nullptr) ? 1 : 0;
   p.ep = L.ep;
   p.ep.P = g.records;
   p.ep.run = nullptr;
   p.ep.q_in_epilogue = 0;   // q-warps (ep.q_warps) or the standalone stream reduce q
   // The tensor-core path exists for bf16 inputs; draft logits share the dtype.
-  auto kern = g.K > 1 ? lmhead_tc_kernel<__nv_bfloat16, true>
-                      : lmhead_tc_kernel<__nv_bfloat16, false>;
+  auto kern = g.rowown ? lmhead_tc_kernel<__nv_bfloat16, true, true>
+               : g.K > 1 ? lmhead_tc_kernel<__nv_bfloat16, true, false>
+                         : lmhead_tc_kernel<__nv_bfloat16, false, false>;
   // The shared-memory opt-in is set once per device, build and size.
-  static int smem_set[kMaxDevices][2] = {{0}};
+  static int smem_set[kMaxDevices][3] = {{0}};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const int which = g.K > 1 ? 1 : 0;
+  const int which = g.rowown ? 2 : g.K > 1 ? 1 : 0;
   if (dev < 0 || dev >= kMaxDevices || smem_set[dev][which] != g.smem_bytes) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, g.smem_bytes);
     if (e != cudaSuccess) return e;
@@ -701,7 +895,8 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kern, *L.tmap_w, *L.tmap_h, p);
+  return cudaLaunchKernelEx(&cfg, kern, *L.tmap_w, *L.tmap_h,
+                            L.tmap_z != nullptr ? *L.tmap_z : *L.tmap_w, p);
 }
 
 }  // namespace specdec

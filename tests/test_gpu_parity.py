@@ -77,6 +77,10 @@ def test_tiny_fp32_sampling(seed):
     (16, 4, 200, 2049, 0.9),    # M = 80: cluster pairs with 2-D boxes (d % 64 != 0), odd tile count
     (16, 4, 128, 1920, 1.1),    # M = 80: cluster pairs with 3-D boxes, 15 tiles (one past the end)
     (40, 4, 64, 3000, 1.0),     # M = 200: one token tile of 208, clusters, q from its own kernel
+    (64, 3, 128, 2049, 0.9),    # M = 256: tokens on the MMA's M side, stream-K, V % 4 != 0
+    (64, 3, 200, 1000, 1.0),    # M = 256, tokens on M with 2-D boxes and a ragged k-slice
+    (100, 4, 64, 3001, 1.0),    # M = 500: two token tiles of 256 on M, the last one partial
+    (128, 3, 192, 1024, 1.2),   # M = 512: two full token tiles on M, vector logit stores
 ])
 def test_bf16_small_shapes(mode, B, gamma, d, V, T):
     w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, temperature=T, sigma=0.4)

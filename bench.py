@@ -280,12 +280,18 @@ def run_ours(args, world, rank, local):
     t_tc = w.flops() / (peaks["bf16_tflops"] * 1e12)
     tensor_bound = t_tc > t_hbm
     if tensor_bound:
+        # The kernel is timed inside a step loop that runs for seconds: the
+        # sustained (power-capped) GEMM rate is its ceiling; the burst rate
+        # is kept beside it.
         achieved = w.flops() / lm_avg_s / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
-                "unit": "TFLOP/s"}
+        sustained = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+        roof = {"bound": "tensor", "achieved": achieved, "peak": sustained,
+                "unit": "TFLOP/s", "peak_kind": "sustained bf16 GEMM",
+                "frac_of_burst": achieved / peaks["bf16_tflops"]}
     else:
         achieved = lm_bytes / lm_avg_s / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "peak_kind": "copy bandwidth"}
     roof["frac"] = roof["achieved"] / roof["peak"]
     roof["traffic"] = recorded_traffic(args.workload, args.mode)
     roof["kernel"] = "lmhead_tc_kernel"
@@ -322,7 +328,9 @@ def run_ours(args, world, rank, local):
         "committed_tokens_per_s": steps_per_s * tokens_per_step,
         "mean_tokens_per_step": tokens_per_step,
         "step_roofline": {"time_us": max(t_hbm, t_tc) * 1e6, "frac": max(t_hbm, t_tc) / step_s,
-                          "bound": "tensor" if tensor_bound else "hbm"},
+                          "bound": "tensor" if tensor_bound else "hbm",
+                          "frac_sustained": max(t_hbm, w.flops() / (peaks.get(
+                              "bf16_tflops_sustained", peaks["bf16_tflops"]) * 1e12)) / step_s},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": e2e,

@@ -182,15 +182,11 @@ def time_oracle(w, inp, mode, budget_s: float, min_steps: int = 1):
 
 # Draft rows up to which the LM-head kernel reduces q itself; beyond, the
 # library runs its standalone q-statistics kernel first (kQWarpMaxRows).
-Q_WARP_MAX_ROWS = 16
 
 
 def kernels_per_step(w, mode) -> int:
-    """Library kernels one step launches: LM head, accept, (sample), (q stats)."""
-    if mode != wl.SAMPLE:
-        return 2
-    q_stream = w.dtype == "bf16" and w.B * w.gamma > Q_WARP_MAX_ROWS
-    return 3 + (1 if q_stream else 0)
+    """Library kernels one step launches: LM head, accept, (sample)."""
+    return 3 if mode == wl.SAMPLE else 2
 
 
 # ------------------------------------------------------------ our arm --

@@ -202,17 +202,14 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   ep.pq = pq;
   ep.run = nullptr;
   ep.q_in_epilogue = 1;
-  // Many draft rows: reduce q in its own stream before the LM head, which
-  // then skips its q-warps.
+  // Many draft rows: the LM-head kernel's streamer warps reduce whole rows
+  // (records of kQChunk columns) instead of the per-tile q-warps.
   const bool q_stream = sample && dtype == SPECDEC_BF16 && B * gamma > kQWarpMaxRows;
   ep.q_warps = q_stream ? 0 : 1;
-  int Pq = 0;
-  if (q_stream) {
-    if (launch_qstats(static_cast<const __nv_bfloat16*>(draft_logits), B * gamma, V, c, pq,
-                      stream) != cudaSuccess)
-      return SPECDEC_ERR_CUDA;
-    Pq = (V + kQChunk - 1) / kQChunk;
-  }
+  ep.q_stream = q_stream ? 1 : 0;
+  const int Pq = q_stream ? (V + kQChunk - 1) / kQChunk : 0;
+  ep.Pq = Pq;
+  ep.q_vec = (V % 8 == 0 && ((uintptr_t)draft_logits & 15u) == 0) ? 1 : 0;
 
   if (ex.ev0 && cudaEventRecord(ex.ev0, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
   cudaError_t e;
@@ -459,6 +456,9 @@ int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void*
   ep.run = nullptr;
   ep.q_in_epilogue = 0;
   ep.q_warps = 0;
+  ep.q_stream = 0;
+  ep.Pq = 0;
+  ep.q_vec = 0;
   TcLaunch L;
   L.tmap_w = &tw;
   L.tmap_h = &th;

@@ -16,7 +16,7 @@ constexpr int kBlockK = 64;         // bf16 per 128-byte swizzled smem row
 constexpr int kMaxBT = 256;         // token rows per tile (MMA N) at most
 constexpr int kChunkV = 4096;       // residual-sampler chunk (256 threads x 16)
 constexpr int kMaxVocab = 1 << 22;  // V limit: the sampler stages 1024 chunk sums
-constexpr int kQChunk = 8192;       // draft-logit columns per q record (standalone stream)
+constexpr int kQChunk = 8192;       // draft-logit columns per streamed q record
 constexpr int kQWarpMaxRows = 16;   // draft rows up to which the LM-head q-warps reduce q
 constexpr int kSampleThreads = 256;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -635,7 +635,10 @@ struct EpiParams {
   RedSlot* run;            // shared memory [M]: fold tiles into one record per
                            // row and CTA (NULL: one record per row and tile)
   int q_in_epilogue;       // 1: the epilogue also reduces the draft logits
-  int q_warps;             // 1: the LM-head kernel's q-warps reduce them
+  int q_warps;             // 1: the LM-head kernel's q-warps reduce them per tile
+  int q_stream;            // 1: its streamer warps reduce them per (row, kQChunk columns)
+  int Pq;                  // q records per draft row when streamed: ceil(V / kQChunk)
+  int q_vec;               // streamed rows allow 16-byte loads (V % 8 == 0, aligned base)
 };
 
 __device__ __forceinline__ void redslot_merge(RedSlot& a, const RedSlot& o, float c) {

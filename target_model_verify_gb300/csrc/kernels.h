@@ -34,11 +34,6 @@ cudaError_t launch_lmhead_f32(const float* hidden, const float* W, int d, const 
 // A tag that no earlier call in this process used.
 unsigned long long next_call_epoch();
 
-// q records straight from the draft logits: one (max, sum) per draft row
-// and kQChunk columns, at pq[row * ceil(V / kQChunk) + chunk].
-cudaError_t launch_qstats(const __nv_bfloat16* dl, int n_rows, int V, float c, PartialQ* pq,
-                          cudaStream_t stream);
-
 // Combine the partials, apply the acceptance rule, write the kept prefix.
 struct AcceptLaunch {
   int B, gamma, V, P, Pq, mode, dl_bf16;   // P, Pq: records per p row and per q row

@@ -67,6 +67,7 @@ constexpr int kThreads = 448;
 constexpr int kEpiThreads = 256;   // warps 2-9
 constexpr int kQWarp0 = 10;        // first q-warp
 constexpr int kQRowsInFlight = 8;
+constexpr int kQStreamWarps = 3;    // streamer q-warps: 10-12 (warp 13 shares the MMA issuer's scheduler)
 constexpr int kStageA = kBlockV * kBlockK * 2;   // 16 KB of W per stage
 constexpr int kMaxStagesC1 = 10;   // stage caps by slices per stage (measured)
 constexpr int kMaxStagesC2 = 4;
@@ -147,6 +148,68 @@ struct PieceIter {
     return true;
   }
 };
+
+// q statistics streamed by spare warps: one (max, sum exp2) record per draft
+// row and kQChunk columns, 16-byte loads (8 bf16) with 8 in flight per lane.
+__device__ __forceinline__ void fold8(float& m, float& s, const uint4& u, float c) {
+  const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&u);
+  float x[8];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float2 f = __bfloat1622float2(h[k]);
+    x[2 * k] = f.x;
+    x[2 * k + 1] = f.y;
+  }
+  float mx = x[0];
+#pragma unroll
+  for (int k = 1; k < 8; ++k) mx = fmaxf(mx, x[k]);
+  const float mm = fmaxf(m, mx);
+  if (mm == -INFINITY) return;   // nothing seen yet: (m, s) stays (-inf, 0)
+  float acc = m == -INFINITY ? 0.f : s * exp2f((m - mm) * c);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc += exp2f((x[k] - mm) * c);
+  m = mm;
+  s = acc;
+}
+
+__device__ __forceinline__ PartialQ q_chunk_stats(const __nv_bfloat16* __restrict__ dl, int r,
+                                                  int chunk, int V, float c, bool vec) {
+  constexpr int kInFlight = 8;
+  const int lane = threadIdx.x & 31;
+  const int c0 = chunk * kQChunk;
+  const int c1 = min(V, c0 + kQChunk);
+  const __nv_bfloat16* row = dl + (size_t)r * V;
+  float m = -INFINITY, s = 0.f;
+  if (vec) {
+    const uint4* base = reinterpret_cast<const uint4*>(row + c0);
+    const int n8 = (c1 - c0) / 8;
+    for (int t0 = lane; t0 < n8; t0 += 32 * kInFlight) {
+      uint4 u[kInFlight];
+#pragma unroll
+      for (int k = 0; k < kInFlight; ++k) {
+        const int t = t0 + 32 * k;
+        u[k] = t < n8 ? __ldcs(base + t) : make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+      }
+#pragma unroll
+      for (int k = 0; k < kInFlight; ++k) fold8(m, s, u[k], c);
+    }
+  } else {
+    for (int v = c0 + lane; v < c1; v += 32) {
+      const float x = __bfloat162float(row[v]);
+      const float mm = fmaxf(m, x);
+      if (mm == -INFINITY) continue;
+      s = (m == -INFINITY ? 0.f : s * exp2f((m - mm) * c)) + exp2f((x - mm) * c);
+      m = mm;
+    }
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    osm_merge(m, s, m2, s2, c);
+  }
+  return PartialQ{m, s};
+}
 
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
@@ -366,7 +429,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp >= kQWarp0) {
     // ---------------------------------------------------------- q-warps --
-    if (p.ep.sample && p.ep.q_warps) {
+    if (p.ep.q_stream && warp < kQWarp0 + kQStreamWarps) {
+      // Many draft rows: stream them whole, (row, kQChunk-column chunk)
+      // items dealt across the grid, while the tensor cores work. The warp
+      // on the MMA issuer's scheduler (warp 13) stays out of it.
+      const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(p.ep.dl);
+      const int g1 = p.gamma + 1;
+      const int n_draft = (p.M / g1) * p.gamma + min(p.M % g1, p.gamma);
+      const long long n_items = (long long)n_draft * p.ep.Pq;
+      const int ns = gridDim.x * kQStreamWarps;
+      for (long long it = (long long)blockIdx.x * kQStreamWarps + (warp - kQWarp0); it < n_items;
+           it += ns) {
+        const int r = (int)(it / p.ep.Pq);
+        const int chunk = (int)(it - (long long)r * p.ep.Pq);
+        const PartialQ q = q_chunk_stats(dl, r, chunk, p.V, p.ep.c, p.ep.q_vec != 0);
+        if (lane == 0) p.ep.pq[(size_t)r * p.ep.Pq + chunk] = q;
+      }
+    } else if (p.ep.sample && p.ep.q_warps) {
       const int qw = warp - kQWarp0;
       const int g1 = p.gamma + 1;
       const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(p.ep.dl);

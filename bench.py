@@ -189,6 +189,29 @@ def kernels_per_step(w, mode) -> int:
     return 3 if mode == wl.SAMPLE else 2
 
 
+# ------------------------------------------------------ multi-rank glue --
+# One process per GPU, each verifying its own batch (independent sequences:
+# no collective on the data path). These three are the only cross-rank
+# steps, and run unchanged on CPU ranks over gloo.
+
+def rank_seed(seed: int, rank: int) -> int:
+    """Each rank draws its own synthetic batch."""
+    return seed + rank
+
+
+def reduce_max_ms(elapsed_ms: float, world: int, device) -> float:
+    """The slowest rank's timed region (all ranks get it)."""
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(world: int, K: int, max_ms: float) -> float:
+    """Steps of all ranks divided by the slowest rank's time."""
+    return world * K / (max_ms / 1e3)
+
+
 # ------------------------------------------------------------ our arm --
 
 def run_ours(args, world, rank, local):
@@ -201,7 +224,7 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=device)
     w = wl.get(args.workload)
     mode = wl.SAMPLE if args.mode == "sample" else wl.GREEDY
-    inp = wl.generate(w, args.seed + rank, device=device)
+    inp = wl.generate(w, rank_seed(args.seed, rank), device=device)
     dl = inp["draft_logits"] if mode == wl.SAMPLE else None
     ws = tv.alloc_workspace(w.B, w.gamma, w.d, w.V, inp["hidden"].dtype, mode, device=device)
     K, Wm = args.steps, args.warmup
@@ -250,10 +273,7 @@ def run_ours(args, world, rank, local):
     if st != 0:
         raise RuntimeError(f"device status {st}: {tv.status_string(st)}")
 
-    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    max_ms = float(t.item())
+    max_ms = reduce_max_ms(elapsed_ms, world, device)
     nacc = naccs[Wm:].double()
     tokens_per_step = float((nacc + 1).sum(dim=1).mean().item())
 
@@ -267,7 +287,7 @@ def run_ours(args, world, rank, local):
         return
 
     peaks, peak_kind = load_peaks()
-    steps_per_s = world * K / (max_ms / 1e3)
+    steps_per_s = whole_job_value(world, K, max_ms)
     lm_avg_s = float(np.mean(lm_ms)) / 1e3
     step_s = max_ms / 1e3 / K
     bytes_alg = w.algorithmic_bytes(mode)

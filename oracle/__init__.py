@@ -16,12 +16,17 @@ What it computes, and where the pages fix it:
   "推测解码" (world.lapla.si/zh/specdec), sections 留下对的，换掉错的 and
   通过的规则; greedy: maxstudionews.com article 1664 (the verify paragraph)
   and "推测解码", section 先让小模型猜.
+* ``tree``     -- tree verification: the same rule at every fork of a token
+  tree (siblings in order, the residual renormalised after each rejection),
+  "推测解码", section 不要第二个模型; a chain-shaped tree is the chain step.
 * ``formulas`` -- the closed forms the same page prints: tokens per weight
   read, speedup, arithmetic overhead (sections 接受率 α, 快多少,
   用的是闲着的算术).
 
-Pins (tests/test_oracle_pins.py) tie every function to something other than
-itself: a library Philox (triton's interpreter), brute-force loops, exact
-enumeration over all 2^24 uniform values, chi-square and binomial bounds,
-and the numbers the page prints. No function here is "parity unpinned".
+Pins (tests/test_oracle_pins.py, tests/test_oracle_tree_pins.py) tie every
+function to something other than itself: a library Philox (triton's
+interpreter), brute-force loops, exact enumeration over all 2^24 uniform
+values, exact rational enumeration of the tree rule's output law, chi-square
+and binomial bounds, and the numbers the page prints. No function here is
+"parity unpinned".
 """

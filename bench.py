@@ -163,29 +163,36 @@ def host_cores() -> int:
 def oracle_inputs(inp: dict, mode: int):
     h = inp["hidden"].float().cpu().double().numpy()
     W = inp["W_lm"].float().cpu().double().numpy()
-    x = inp["draft_tokens"].cpu().numpy().astype(np.int64)
+    x = inp["node_tokens" if "node_tokens" in inp else "draft_tokens"].cpu().numpy().astype(np.int64)
     dl = inp["draft_logits"].float().cpu().double().numpy() if mode == wl.SAMPLE else None
     return h, W, x, dl
 
 
+def oracle_step(w, h, W, x, dl, seed, mode):
+    """One step of the fp64 oracle (chain or tree) on converted inputs."""
+    if w.tree is not None:
+        from oracle import tree as ot
+        return ot.verify_tree(h, W, w.tree, x, dl, w.temperature, seed, mode)
+    from oracle import verify as ov
+    return ov.verify(h, W, x, dl, w.temperature, seed, mode)
+
+
 def time_oracle(w, inp, mode, budget_s: float, min_steps: int = 1):
     """Full oracle steps on the host cores until the budget is used."""
-    from oracle import verify as ov
     h, W, x, dl = oracle_inputs(inp, mode)
     n = 0
     t0 = time.perf_counter()
     while n < min_steps or time.perf_counter() - t0 < budget_s:
-        ov.verify(h, W, x, dl, w.temperature, 1000 + n, mode)
+        oracle_step(w, h, W, x, dl, 1000 + n, mode)
         n += 1
     return n / (time.perf_counter() - t0), n
 
 
-# Draft rows up to which the LM-head kernel reduces q itself; beyond, the
-# library runs its standalone q-statistics kernel first (kQWarpMaxRows).
-
-
 def kernels_per_step(w, mode) -> int:
-    """Library kernels one step launches: LM head, accept, (sample)."""
+    """Library kernels one step launches: LM head, accept, (sample); for a
+    tree, LM head and the tree walk."""
+    if w.tree is not None:
+        return 2
     return 3 if mode == wl.SAMPLE else 2
 
 
@@ -224,11 +231,17 @@ def run_ours(args, world, rank, local):
         dist.init_process_group("nccl", device_id=device)
     w = wl.get(args.workload)
     mode = wl.SAMPLE if args.mode == "sample" else wl.GREEDY
-    inp = wl.generate(w, rank_seed(args.seed, rank), device=device)
+    is_tree = w.tree is not None
+    gen = wl.generate_tree if is_tree else wl.generate
+    inp = gen(w, rank_seed(args.seed, rank), device=device)
     dl = inp["draft_logits"] if mode == wl.SAMPLE else None
-    ws = tv.alloc_workspace(w.B, w.gamma, w.d, w.V, inp["hidden"].dtype, mode, device=device)
+    if is_tree:
+        ws = tv.alloc_tree_workspace(w.B, w.N, w.d, w.V, inp["hidden"].dtype, mode, device=device)
+    else:
+        ws = tv.alloc_workspace(w.B, w.gamma, w.d, w.V, inp["hidden"].dtype, mode, device=device)
     K, Wm = args.steps, args.warmup
-    outs = torch.empty(K + Wm, w.B, w.gamma + 1, dtype=torch.int32, device=device)
+    outs = torch.empty(K + Wm, w.B, w.N, dtype=torch.int32, device=device)
+    nodes = torch.empty(K + Wm, w.B, w.N, dtype=torch.int32, device=device) if is_tree else None
     naccs = torch.empty(K + Wm, w.B, dtype=torch.int32, device=device)
     ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
     ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
@@ -237,9 +250,14 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
 
     def step(i, events=None):
-        tv.verify(inp["hidden"], inp["W_lm"], inp["draft_tokens"], dl, w.temperature,
-                  args.seed * 1_000_003 + i, mode, out_tokens=outs[i], n_accepted=naccs[i],
-                  workspace=ws, events=events)
+        if is_tree:
+            tv.verify_tree(inp["hidden"], inp["W_lm"], w.tree, inp["node_tokens"], dl,
+                           w.temperature, args.seed * 1_000_003 + i, mode, out_tokens=outs[i],
+                           out_nodes=nodes[i], n_accepted=naccs[i], workspace=ws, events=events)
+        else:
+            tv.verify(inp["hidden"], inp["W_lm"], inp["draft_tokens"], dl, w.temperature,
+                      args.seed * 1_000_003 + i, mode, out_tokens=outs[i], n_accepted=naccs[i],
+                      workspace=ws, events=events)
 
     sampler = ClockSampler(device.index) if rank == 0 else None
     time.sleep(0.6 if sampler else 0)
@@ -291,7 +309,8 @@ def run_ours(args, world, rank, local):
     lm_avg_s = float(np.mean(lm_ms)) / 1e3
     step_s = max_ms / 1e3 / K
     bytes_alg = w.algorithmic_bytes(mode)
-    lm_bytes = bytes_alg - w.B * w.gamma * 4          # the LM-head kernel does not read x
+    n_tok = w.B * ((w.N - 1) if w.tree is not None else w.gamma)
+    lm_bytes = bytes_alg - n_tok * 4                  # the LM-head kernel does not read the tokens
     t_hbm = bytes_alg / (peaks["hbm_gbs"] * 1e9)
     t_tc = w.flops() / (peaks["bf16_tflops"] * 1e12)
     tensor_bound = t_tc > t_hbm
@@ -339,6 +358,8 @@ def run_ours(args, world, rank, local):
         "data": "synthetic (seeded; random-init LM head)",
         "config": {"workload": args.workload, "B": w.B, "gamma": w.gamma, "d": w.d, "V": w.V,
                    "mode": args.mode, "temperature": w.temperature,
+                   **({"tree_nodes": w.N, "tree_depth": tree_depth(w.tree)}
+                      if w.tree is not None else {}),
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "l2": "inputs larger than L2 (W_lm exceeds the 129 MB L2), no flush"},
         "committed_tokens_per_s": steps_per_s * tokens_per_step,
@@ -358,8 +379,52 @@ def run_ours(args, world, rank, local):
         torch.distributed.destroy_process_group()
 
 
+def tree_depth(parent) -> int:
+    depth = [0] * len(parent)
+    for n in range(1, len(parent)):
+        depth[n] = depth[parent[n]] + 1
+    return max(depth)
+
+
+def run_e2e_tree(tv, w, inp, mode, K, Wm, args, device):
+    """Tree steps through the public API from pinned host tensors: copy the
+    step's inputs in, verify, read the results back, every step."""
+    host = {k: inp[k].cpu().pin_memory() for k in ("hidden", "node_tokens", "draft_logits")}
+    dev = {k: torch.empty_like(v, device=device) for k, v in host.items()}
+    out = torch.empty(w.B, w.N, dtype=torch.int32, pin_memory=True)
+    nod = torch.empty(w.B, w.N, dtype=torch.int32, pin_memory=True)
+    nacc = torch.empty(w.B, dtype=torch.int32, pin_memory=True)
+    ws = tv.alloc_tree_workspace(w.B, w.N, w.d, w.V, inp["hidden"].dtype, mode, device=device)
+    names = ("hidden", "node_tokens") + (("draft_logits",) if mode == wl.SAMPLE else ())
+
+    def step(i):
+        for k in names:
+            dev[k].copy_(host[k], non_blocking=True)
+        o, n, a = tv.verify_tree(dev["hidden"], inp["W_lm"], w.tree, dev["node_tokens"],
+                                 dev["draft_logits"] if mode == wl.SAMPLE else None,
+                                 w.temperature, i, mode, workspace=ws)
+        out.copy_(o, non_blocking=True)
+        nod.copy_(n, non_blocking=True)
+        nacc.copy_(a, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for i in range(Wm):
+        step(i)
+    n = max(1, min(K, 2000))
+    t0 = time.perf_counter()
+    for i in range(n):
+        step(Wm + i)
+    dt = time.perf_counter() - t0
+    h2d = sum(host[k].numel() * host[k].element_size() for k in names)
+    d2h = out.numel() * 4 + nod.numel() * 4 + nacc.numel() * 4
+    return {"value": n / dt, "unit": "steps/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": n}
+
+
 def run_e2e(tv, w, inp, mode, K, Wm, args, device):
     """Same metric through the host-pointer entry point, copies included."""
+    if w.tree is not None:
+        return run_e2e_tree(tv, w, inp, mode, K, Wm, args, device)
     host = {k: v.cpu().pin_memory() for k, v in inp.items() if k != "W_lm"}
     hl = host["draft_logits"] if mode == wl.SAMPLE else None
     out = torch.empty(w.B, w.gamma + 1, dtype=torch.int32, pin_memory=True)
@@ -392,15 +457,14 @@ def run_reference(args, world, rank, local):
     """The fp64 oracle on the host cores, on this arm's workload."""
     if rank != 0:
         return
-    from oracle import verify as ov
     w = wl.get(args.workload)
     mode = wl.SAMPLE if args.mode == "sample" else wl.GREEDY
     device = "cuda" if torch.cuda.is_available() else "cpu"
-    inp = wl.generate(w, args.seed, device=device)
+    inp = (wl.generate_tree if w.tree is not None else wl.generate)(w, args.seed, device=device)
     h, W, x, dl = oracle_inputs(inp, mode)
     # One full step, to size the per-step sample so the run fits the budget.
     t0 = time.perf_counter()
-    ov.verify(h, W, x, dl, w.temperature, 0, mode)
+    oracle_step(w, h, W, x, dl, 0, mode)
     t_full = time.perf_counter() - t0
     n_total = args.steps + args.warmup
     frac = min(1.0, REFERENCE_BUDGET_SECONDS / max(n_total * t_full, 1e-9))
@@ -409,10 +473,10 @@ def run_reference(args, world, rank, local):
     xs = np.minimum(x, Vs - 1)
     dls = dl[..., :Vs] if dl is not None else None
     for i in range(args.warmup):
-        ov.verify(h, Ws, xs, dls, w.temperature, i, mode)
+        oracle_step(w, h, Ws, xs, dls, i, mode)
     t0 = time.perf_counter()
     for k in range(args.steps):
-        ov.verify(h, Ws, xs, dls, w.temperature, args.warmup + k, mode)
+        oracle_step(w, h, Ws, xs, dls, args.warmup + k, mode)
     dt = time.perf_counter() - t0
     scale = Vs / w.V
     value = args.steps * scale / dt

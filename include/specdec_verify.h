@@ -38,8 +38,9 @@
  *     Argument errors are detected on the host before anything is enqueued.
  *     Errors found on the device (draft token out of [0, V), a kernel wait
  *     that timed out) are written to a status word in the workspace; the
- *     affected call then writes n_accepted = -1 and out_tokens = -1 for
- *     every sequence. specdec_read_status() returns that word.
+ *     call then writes n_accepted = -1 and out_tokens = -1 for the affected
+ *     sequences (a token out of range: its sequence; a timeout: every
+ *     sequence). specdec_read_status() returns that word.
  *   - Shapes: B >= 0 (B == 0 returns SPECDEC_OK and touches no pointer),
  *     1 <= gamma <= SPECDEC_MAX_GAMMA,
  *     d >= 1 with d % 8 == 0 for bf16 (rows must be 16-byte aligned),
@@ -57,6 +58,7 @@ extern "C" {
 #endif
 
 #define SPECDEC_MAX_GAMMA 32
+#define SPECDEC_MAX_TREE_NODES 128
 
 /* mode */
 #define SPECDEC_SAMPLE 0
@@ -174,6 +176,53 @@ int specdec_verify_noalloc(const void* hidden, const void* W_lm, const int32_t* 
                            const void* draft_logits, int B, int gamma, int d, int V, int dtype,
                            float temperature, uint64_t seed, int mode, int32_t* out_tokens,
                            int32_t* n_accepted, void* stream);
+
+/*
+ * Tree verification ("推测解码", section 不要第二个模型: guesses arranged as
+ * a tree are checked in one pass, with the acceptance rule applied at every
+ * fork). One tree topology for the whole batch, given by `parent`, a HOST
+ * array of n_nodes int32: parent[0] = -1 (the root, the position after the
+ * committed text) and 0 <= parent[n] < n for n >= 1, so 1 <= n_nodes <=
+ * SPECDEC_MAX_TREE_NODES. Node n >= 1 holds one guessed token.
+ *   hidden       [B, N, d]   dtype   target state after the path root -> n;
+ *                                    p_n = softmax(z_n / T) scores n's children
+ *   W_lm         [V, d]      dtype   LM-head weights
+ *   node_tokens  [B, N]      int32   guessed token of every node (column 0
+ *                                    ignored); in [0, V) else the status word
+ *                                    gets SPECDEC_ERR_TOKEN_RANGE
+ *   draft_logits [B, N, V]   dtype   q_n, the distribution n's children were
+ *                                    drawn from (rows of leaves are read but
+ *                                    unused); may be NULL in greedy mode
+ *   out_tokens   [B, N]      int32   kept path tokens, then the drawn (or argmax)
+ *                                    token, then -1
+ *   out_nodes    [B, N]      int32   kept node indices in path order, then -1
+ *   n_accepted   [B]         int32   number of kept nodes
+ * Sampling rule at node u: children in increasing index; child c is kept iff
+ * r_c * q_u(x_c) <= f(x_c), with f = p_u for the first child and f =
+ * max(0, f - q_u) / S after each rejection (S its sum over the vocabulary);
+ * a kept child becomes the node; otherwise one token is drawn from the last
+ * residual max(0, f - q_u) (or from p_u when u has no children) by the
+ * inversion above. Random draws: child c uses the acceptance uniform of
+ * position c - 1, the draw at depth j the sampling uniform of position j,
+ * so a chain-shaped tree (parent[n] = n - 1) gives the same tokens as
+ * specdec_verify(). Greedy: move to the first child whose token is the
+ * target argmax; else write the argmax. Only dtype SPECDEC_BF16; limits as
+ * specdec_verify() with M = B*N rows. Asynchronous on `stream`.
+ */
+size_t specdec_verify_tree_workspace_size(int B, int n_nodes, int d, int V, int dtype, int mode);
+int specdec_verify_tree(const void* hidden, const void* W_lm, const int32_t* parent,
+                        const int32_t* node_tokens, const void* draft_logits, int B, int n_nodes,
+                        int d, int V, int dtype, float temperature, uint64_t seed, int mode,
+                        int32_t* out_tokens, int32_t* out_nodes, int32_t* n_accepted,
+                        void* workspace, size_t workspace_bytes, void* stream);
+/* specdec_verify_tree() with events around its LM-head kernel (see
+ * specdec_verify_timed). */
+int specdec_verify_tree_timed(const void* hidden, const void* W_lm, const int32_t* parent,
+                              const int32_t* node_tokens, const void* draft_logits, int B,
+                              int n_nodes, int d, int V, int dtype, float temperature,
+                              uint64_t seed, int mode, int32_t* out_tokens, int32_t* out_nodes,
+                              int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                              void* stream, void* lmhead_start_event, void* lmhead_end_event);
 
 /*
  * Reads the device status word of a workspace after synchronising `stream`:

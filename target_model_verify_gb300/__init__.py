@@ -124,6 +124,55 @@ def verify_host(hidden, W_lm, draft_tokens, draft_logits, temperature=1.0, seed=
     return out_tokens, n_accepted
 
 
+def tree_workspace_bytes(B, n_nodes, d, V, dtype=torch.bfloat16, mode=SAMPLE) -> int:
+    return _b.specdec_verify_tree_workspace_size(B, n_nodes, d, V, _DTYPES[dtype], mode)
+
+
+def alloc_tree_workspace(B, n_nodes, d, V, dtype=torch.bfloat16, mode=SAMPLE, device=None):
+    n = tree_workspace_bytes(B, n_nodes, d, V, dtype, mode)
+    if n == 0:
+        raise SpecdecError(_b.SPECDEC_ERR_UNSUPPORTED, "tree_workspace_bytes")
+    return torch.empty(n, dtype=torch.uint8, device=device or "cuda")
+
+
+def verify_tree(hidden, W_lm, parent, node_tokens, draft_logits, temperature=1.0, seed=0,
+                mode=SAMPLE, out_tokens=None, out_nodes=None, n_accepted=None, workspace=None,
+                stream=None, events=None):
+    """Tree verification (see include/specdec_verify.h, specdec_verify_tree).
+
+    hidden [B, N, d] bf16, W_lm [V, d] bf16, parent: N ints (parent[0] = -1,
+    parent[n] < n), node_tokens [B, N] int32, draft_logits [B, N, V] bf16
+    (None allowed in greedy mode). Returns (out_tokens [B, N], out_nodes
+    [B, N], n_accepted [B]), all int32 on the device.
+    """
+    _check_inputs(hidden, W_lm, node_tokens, draft_logits, mode, "cuda")
+    B, N, d = hidden.shape
+    V = W_lm.shape[0]
+    par = torch.as_tensor(list(parent), dtype=torch.int32).contiguous()
+    if par.numel() != N:
+        raise ValueError("parent must have one entry per node")
+    dev = hidden.device
+    if out_tokens is None:
+        out_tokens = torch.empty(B, N, dtype=torch.int32, device=dev)
+    if out_nodes is None:
+        out_nodes = torch.empty(B, N, dtype=torch.int32, device=dev)
+    if n_accepted is None:
+        n_accepted = torch.empty(B, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = alloc_tree_workspace(B, N, d, V, hidden.dtype, mode, device=dev)
+    args = (_ptr(hidden), _ptr(W_lm), _ptr(par), _ptr(node_tokens), _ptr(draft_logits), B, N, d,
+            V, _DTYPES[hidden.dtype], float(temperature), int(seed) & (2 ** 64 - 1), int(mode),
+            _ptr(out_tokens), _ptr(out_nodes), _ptr(n_accepted), _ptr(workspace),
+            workspace.numel(), _stream_ptr(stream))
+    if events is not None:
+        rc = _b.specdec_verify_tree_timed(*args, int(events[0].cuda_event),
+                                          int(events[1].cuda_event))
+    else:
+        rc = _b.specdec_verify_tree(*args)
+    _b._check(rc, "specdec_verify_tree")
+    return out_tokens, out_nodes, n_accepted
+
+
 def read_status(workspace, stream=None) -> int:
     """The device status word of the last call that used `workspace`."""
     return _b.specdec_read_status(_ptr(workspace), _stream_ptr(stream))

@@ -21,6 +21,7 @@ SPECDEC_GREEDY = 1
 SPECDEC_BF16 = 0
 SPECDEC_FP32 = 1
 SPECDEC_MAX_GAMMA = 32
+SPECDEC_MAX_TREE_NODES = 128
 
 SPECDEC_OK = 0
 SPECDEC_ERR_INVALID_ARG = -1
@@ -38,6 +39,8 @@ _sz = ctypes.c_size_t
 
 _CORE = [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _u64, _i, _vp, _vp, _vp, _sz, _vp]
 
+_TREE = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _u64, _i, _vp, _vp, _vp, _vp, _sz, _vp]
+
 _SIGNATURES = {
     "specdec_verify_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "specdec_verify": (_i, _CORE),
@@ -50,6 +53,9 @@ _SIGNATURES = {
     "specdec_status_string": (ctypes.c_char_p, [_i]),
     "specdec_verify_noalloc": (_i, _CORE[:14] + [_vp]),
     "specdec_selftest_wait_timeout": (_i, [_vp, _sz, _vp, ctypes.POINTER(ctypes.c_int32)]),
+    "specdec_verify_tree_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "specdec_verify_tree": (_i, _TREE),
+    "specdec_verify_tree_timed": (_i, _TREE + [_vp, _vp]),
 }
 
 _lib = None
@@ -124,6 +130,19 @@ def specdec_verify_host(*args) -> int:
 def specdec_verify_noalloc(*args) -> int:
     """The verify step with the library's static scratch (no workspace)."""
     return int(lib().specdec_verify_noalloc(*args))
+
+
+def specdec_verify_tree_workspace_size(B, n_nodes, d, V, dtype, mode) -> int:
+    return int(lib().specdec_verify_tree_workspace_size(B, n_nodes, d, V, dtype, mode))
+
+
+def specdec_verify_tree(*args) -> int:
+    """Tree verification (the parent array is a host int32 array)."""
+    return int(lib().specdec_verify_tree(*args))
+
+
+def specdec_verify_tree_timed(*args) -> int:
+    return int(lib().specdec_verify_tree_timed(*args))
 
 
 def specdec_read_status(workspace_ptr: int, stream_ptr: int) -> int:

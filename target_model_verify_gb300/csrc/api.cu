@@ -152,6 +152,45 @@ struct Extras {
   cudaEvent_t ev1 = nullptr;
 };
 
+// The bf16 LM-head stage shared by the chain and tree steps: tensor maps,
+// geometry and the launch. *records = partial records per row it writes.
+int lmhead_stage_bf16(const void* hidden, const void* W, int M, int d, int V, const EpiParams& ep,
+                      int* status, char* ws, size_t off_tickets, size_t off_fix,
+                      unsigned long long epoch, int nsm, cudaStream_t stream, int* records) {
+  const int max_clusters = tc_max_clusters(M, V, d);
+  const TcGeometry g = tc_geometry(M, V, d, nsm, max_clusters);
+  // A CTA of a pair loads its BT/K token rows of all kc slices of a stage.
+  const int h_rows = g.BT / g.K;
+  const int h_slices = g.kc;
+  CUtensorMap tw, th;
+  const bool ok = g.box3d ? (encode_bf16_rows3d(&tw, W, V, d, kBlockV, g.kc) &&
+                             encode_bf16_rows3d(&th, hidden, M, d, h_rows, h_slices))
+                          : (encode_bf16_rows(&tw, W, V, d, kBlockV) &&
+                             encode_bf16_rows(&th, hidden, M, d, h_rows));
+  if (!ok) return SPECDEC_ERR_CUDA;
+  float* z = ep.zout;
+  CUtensorMap tz;
+  const bool ztma = g.rowown && z != nullptr && V % 4 == 0 && ((uintptr_t)z & 15u) == 0 &&
+                    encode_f32_tiles(&tz, z, M, V);
+  TcLaunch L;
+  L.tmap_w = &tw;
+  L.tmap_h = &th;
+  L.tmap_z = ztma ? &tz : nullptr;
+  L.M = M;
+  L.V = V;
+  L.d = d;
+  L.gamma = ep.gamma;
+  L.status = status;
+  L.fix = reinterpret_cast<float*>(ws + off_fix);
+  L.fix_tickets = reinterpret_cast<unsigned long long*>(ws + off_tickets);
+  L.epoch = epoch;
+  L.max_clusters = max_clusters;
+  L.withhold_loads = 0;
+  L.ep = ep;
+  *records = g.records;
+  return launch_lmhead_tc(L, nsm, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
+
 int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
                 const void* draft_logits, int B, int gamma, int d, int V, int dtype, float T,
                 uint64_t seed, int mode, int32_t* out_tokens, int32_t* n_accepted, void* workspace,
@@ -207,49 +246,20 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   const bool q_stream = sample && dtype == SPECDEC_BF16 && B * gamma > kQWarpMaxRows;
   ep.q_warps = q_stream ? 0 : 1;
   ep.q_stream = q_stream ? 1 : 0;
+  ep.n_qrows = B * gamma;
   const int Pq = q_stream ? (V + kQChunk - 1) / kQChunk : 0;
   ep.Pq = Pq;
   ep.q_vec = (V % 8 == 0 && ((uintptr_t)draft_logits & 15u) == 0) ? 1 : 0;
 
   if (ex.ev0 && cudaEventRecord(ex.ev0, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
-  cudaError_t e;
   if (dtype == SPECDEC_BF16) {
-    const int max_clusters = tc_max_clusters(pl.M, V, d);
-    const TcGeometry g = tc_geometry(pl.M, V, d, nsm, max_clusters);
-    // A CTA of a pair loads its BT/K token rows of all kc slices of a stage.
-    const int h_rows = g.BT / g.K;
-    const int h_slices = g.kc;
-    CUtensorMap tw, th;
-    const bool ok = g.box3d ? (encode_bf16_rows3d(&tw, W, V, d, kBlockV, g.kc) &&
-                               encode_bf16_rows3d(&th, hidden, pl.M, d, h_rows, h_slices))
-                            : (encode_bf16_rows(&tw, W, V, d, kBlockV) &&
-                               encode_bf16_rows(&th, hidden, pl.M, d, h_rows));
-    if (!ok) return SPECDEC_ERR_CUDA;
-    CUtensorMap tz;
-    const bool ztma = g.rowown && z != nullptr && V % 4 == 0 && ((uintptr_t)z & 15u) == 0 &&
-                      encode_f32_tiles(&tz, z, pl.M, V);
-    TcLaunch L;
-    L.tmap_w = &tw;
-    L.tmap_h = &th;
-    L.tmap_z = ztma ? &tz : nullptr;
-    L.M = pl.M;
-    L.V = V;
-    L.d = d;
-    L.gamma = gamma;
-    L.status = status;
-    L.fix = reinterpret_cast<float*>(ws + pl.off_fix);
-    L.fix_tickets = reinterpret_cast<unsigned long long*>(ws + pl.off_tickets);
-    L.epoch = epoch;
-    L.max_clusters = max_clusters;
-    L.withhold_loads = 0;
-    L.ep = ep;
-    P = g.records;
-    e = launch_lmhead_tc(L, nsm, stream);
-  } else {
-    e = launch_lmhead_f32(static_cast<const float*>(hidden), static_cast<const float*>(W), d, ep,
-                          status, stream);
+    rc = lmhead_stage_bf16(hidden, W, pl.M, d, V, ep, status, ws, pl.off_tickets, pl.off_fix, epoch,
+                           nsm, stream, &P);
+    if (rc != SPECDEC_OK) return rc;
+  } else if (launch_lmhead_f32(static_cast<const float*>(hidden), static_cast<const float*>(W), d,
+                               ep, status, stream) != cudaSuccess) {
+    return SPECDEC_ERR_CUDA;
   }
-  if (e != cudaSuccess) return SPECDEC_ERR_CUDA;
   if (ex.ev1 && cudaEventRecord(ex.ev1, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
 
   AcceptLaunch A;
@@ -307,6 +317,47 @@ size_t host_staging_bytes(int B, int gamma, int d, int V, int dtype, int mode) {
   if (mode == SPECDEC_SAMPLE) n += align_up((size_t)B * gamma * V * e);   // draft logits
   n += align_up(M * 4) + align_up((size_t)B * 4);                   // outputs
   return n;
+}
+
+// ---------------------------------------------------------------- tree --
+
+struct TreePlan {
+  int M, P, Pq;
+  size_t off_tickets, off_pp, off_pq, off_z, off_fix, total;
+};
+
+int check_tree_shape(int B, int N, int d, int V, int dtype, int mode) {
+  if (dtype != SPECDEC_BF16 && dtype != SPECDEC_FP32) return SPECDEC_ERR_INVALID_ARG;
+  if (mode != SPECDEC_SAMPLE && mode != SPECDEC_GREEDY) return SPECDEC_ERR_INVALID_ARG;
+  if (dtype != SPECDEC_BF16) return SPECDEC_ERR_UNSUPPORTED;
+  if (B < 0 || N < 1 || N > SPECDEC_MAX_TREE_NODES || d < 1 || d % 8 != 0 || V < 1 ||
+      V > kMaxVocab)
+    return SPECDEC_ERR_UNSUPPORTED;
+  const long long M = (long long)B * N;
+  if (M * (long long)V >= (1ll << 31)) return SPECDEC_ERR_UNSUPPORTED;
+  if ((M + 15) / 16 > 65535) return SPECDEC_ERR_UNSUPPORTED;
+  return SPECDEC_OK;
+}
+
+TreePlan make_tree_plan(int B, int N, int d, int V, int mode) {
+  TreePlan p;
+  p.M = B * N;
+  p.P = (V + kBlockV - 1) / kBlockV + 2;
+  p.Pq = (V + kQChunk - 1) / kQChunk;
+  const bool sample = mode == SPECDEC_SAMPLE;
+  size_t off = align_up(sizeof(WsHeader));
+  p.off_tickets = off;
+  off = align_up(off + sizeof(unsigned long long) * kFixSlots);
+  p.off_pp = off;
+  off = align_up(off + sizeof(PartialP) * (size_t)p.M * p.P);
+  p.off_pq = off;
+  if (sample) off = align_up(off + sizeof(PartialQ) * (size_t)p.M * p.Pq);
+  p.off_z = off;
+  if (sample) off = align_up(off + sizeof(float) * (size_t)p.M * V);
+  p.off_fix = off;
+  off = align_up(off + sizeof(float) * tc_fix_floats(p.M, V, d));
+  p.total = off;
+  return p;
 }
 
 }  // namespace
@@ -457,6 +508,7 @@ int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void*
   ep.q_in_epilogue = 0;
   ep.q_warps = 0;
   ep.q_stream = 0;
+  ep.n_qrows = 0;
   ep.Pq = 0;
   ep.q_vec = 0;
   TcLaunch L;
@@ -479,6 +531,118 @@ int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void*
   if (cudaMemcpy(status, ws, sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
     return SPECDEC_ERR_CUDA;
   return SPECDEC_OK;
+}
+
+size_t specdec_verify_tree_workspace_size(int B, int n_nodes, int d, int V, int dtype, int mode) {
+  if (check_tree_shape(B, n_nodes, d, V, dtype, mode) != SPECDEC_OK) return 0;
+  return make_tree_plan(B, n_nodes, d, V, mode).total;
+}
+
+int specdec_verify_tree_timed(const void* hidden, const void* W_lm, const int32_t* parent,
+                              const int32_t* node_tokens, const void* draft_logits, int B,
+                              int n_nodes, int d, int V, int dtype, float temperature,
+                              uint64_t seed, int mode, int32_t* out_tokens, int32_t* out_nodes,
+                              int32_t* n_accepted, void* workspace, size_t workspace_bytes,
+                              void* stream_ptr, void* lmhead_start_event,
+                              void* lmhead_end_event) {
+  int rc = check_tree_shape(B, n_nodes, d, V, dtype, mode);
+  if (rc != SPECDEC_OK) return rc;
+  const int N = n_nodes;
+  if (!parent) return SPECDEC_ERR_INVALID_ARG;
+  // The topology: parent[0] = -1, parent[n] an earlier node; children are
+  // linked in increasing index.
+  TreeLaunch T;
+  if (parent[0] != -1) return SPECDEC_ERR_INVALID_ARG;
+  for (int n = 0; n < SPECDEC_MAX_TREE_NODES; ++n)
+    T.first_child[n] = T.next_sibling[n] = T.parent[n] = -1;
+  for (int n = N - 1; n >= 1; --n) {
+    const int pa = parent[n];
+    if (pa < 0 || pa >= n) return SPECDEC_ERR_INVALID_ARG;
+    T.parent[n] = (int16_t)pa;
+    T.next_sibling[n] = T.first_child[pa];
+    T.first_child[pa] = (int16_t)n;
+  }
+  if (B == 0) return SPECDEC_OK;
+  const bool sample = mode == SPECDEC_SAMPLE;
+  if (!hidden || !W_lm || !node_tokens || !out_tokens || !out_nodes || !n_accepted)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (sample && (!draft_logits || !(temperature > 0.f) || !std::isfinite(temperature)))
+    return SPECDEC_ERR_INVALID_ARG;
+  if (((uintptr_t)hidden & 15u) != 0 || ((uintptr_t)W_lm & 15u) != 0)
+    return SPECDEC_ERR_INVALID_ARG;
+  const TreePlan pl = make_tree_plan(B, N, d, V, mode);
+  if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || workspace_bytes < pl.total)
+    return SPECDEC_ERR_WORKSPACE;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SPECDEC_ERR_CUDA;
+
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  PartialP* pp = reinterpret_cast<PartialP*>(ws + pl.off_pp);
+  PartialQ* pq = reinterpret_cast<PartialQ*>(ws + pl.off_pq);
+  float* z = sample ? reinterpret_cast<float*>(ws + pl.off_z) : nullptr;
+  const float c = sample ? kLog2e / temperature : kLog2e;
+
+  EpiParams ep;
+  ep.M = pl.M;
+  ep.V = V;
+  ep.gamma = 1;               // unused: no per-tile q-warps for trees
+  ep.P = 0;
+  ep.c = c;
+  ep.sample = sample ? 1 : 0;
+  ep.want_argmax = sample ? 0 : 1;
+  ep.zout = z;
+  ep.dl = draft_logits;
+  ep.pp = pp;
+  ep.pq = pq;
+  ep.run = nullptr;
+  ep.q_in_epilogue = 0;
+  ep.q_warps = 0;
+  // Every node's draft row is reduced by the LM-head kernel's streamer warps.
+  ep.q_stream = sample ? 1 : 0;
+  ep.n_qrows = pl.M;
+  ep.Pq = pl.Pq;
+  ep.q_vec = (V % 8 == 0 && ((uintptr_t)draft_logits & 15u) == 0) ? 1 : 0;
+  int P = 0;
+  cudaEvent_t ev0 = static_cast<cudaEvent_t>(lmhead_start_event);
+  cudaEvent_t ev1 = static_cast<cudaEvent_t>(lmhead_end_event);
+  if (ev0 && cudaEventRecord(ev0, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  rc = lmhead_stage_bf16(hidden, W_lm, pl.M, d, V, ep, status, ws, pl.off_tickets, pl.off_fix,
+                         next_call_epoch(), nsm, stream, &P);
+  if (rc != SPECDEC_OK) return rc;
+  if (ev1 && cudaEventRecord(ev1, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+
+  T.B = B;
+  T.N = N;
+  T.V = V;
+  T.P = P;
+  T.Pq = pl.Pq;
+  T.mode = mode;
+  T.vec = (V % 4 == 0 && ((uintptr_t)draft_logits & 7u) == 0) ? 1 : 0;
+  T.c = c;
+  T.seed = seed;
+  T.pp = pp;
+  T.pq = pq;
+  T.z = z;
+  T.dl = static_cast<const __nv_bfloat16*>(draft_logits);
+  T.tok = node_tokens;
+  T.out_tokens = out_tokens;
+  T.out_nodes = out_nodes;
+  T.n_accepted = n_accepted;
+  T.status = status;
+  return launch_tree_walk(T, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
+
+int specdec_verify_tree(const void* hidden, const void* W_lm, const int32_t* parent,
+                        const int32_t* node_tokens, const void* draft_logits, int B, int n_nodes,
+                        int d, int V, int dtype, float temperature, uint64_t seed, int mode,
+                        int32_t* out_tokens, int32_t* out_nodes, int32_t* n_accepted,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  return specdec_verify_tree_timed(hidden, W_lm, parent, node_tokens, draft_logits, B, n_nodes, d,
+                                   V, dtype, temperature, seed, mode, out_tokens, out_nodes,
+                                   n_accepted, workspace, workspace_bytes, stream, nullptr,
+                                   nullptr);
 }
 
 int specdec_read_status(const void* workspace, void* stream, int32_t* status) {

@@ -308,6 +308,22 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
     }
   }
 }
+// Loads from another CTA's shared memory (address from mapa_shared).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ int ld_cluster_s32(uint32_t addr) {
+  int v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release;" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
@@ -637,6 +653,7 @@ struct EpiParams {
   int q_in_epilogue;       // 1: the epilogue also reduces the draft logits
   int q_warps;             // 1: the LM-head kernel's q-warps reduce them per tile
   int q_stream;            // 1: its streamer warps reduce them per (row, kQChunk columns)
+  int n_qrows;             // draft-logit rows the streamer reduces (rows of dl, in order)
   int Pq;                  // q records per draft row when streamed: ceil(V / kQChunk)
   int q_vec;               // streamed rows allow 16-byte loads (V % 8 == 0, aligned base)
 };

@@ -72,6 +72,28 @@ struct SampleLaunch {
 };
 cudaError_t launch_sample(const SampleLaunch& L, cudaStream_t stream);
 
+// Tree verification walk: one cluster of kTreeCluster CTAs per sequence
+// (sampling; the CTAs split the vocabulary) or one CTA (greedy).
+constexpr int kTreeCluster = 8;
+struct TreeLaunch {
+  int B, N, V, P, Pq, mode, vec;
+  float c;
+  uint64_t seed;
+  const PartialP* pp;            // [B*N, P] target records
+  const PartialQ* pq;            // [B*N, Pq] draft records (sampling)
+  const float* z;                // [B*N, V] fp32 logits (sampling)
+  const __nv_bfloat16* dl;       // [B*N, V] draft logits (sampling)
+  const int32_t* tok;            // [B, N] node tokens (column 0 unused)
+  int16_t first_child[SPECDEC_MAX_TREE_NODES];    // -1: none; children in increasing index
+  int16_t next_sibling[SPECDEC_MAX_TREE_NODES];
+  int16_t parent[SPECDEC_MAX_TREE_NODES];         // parent[0] = -1
+  int32_t* out_tokens;           // [B, N]
+  int32_t* out_nodes;            // [B, N]
+  int32_t* n_accepted;           // [B]
+  int* status;
+};
+cudaError_t launch_tree_walk(const TreeLaunch& L, cudaStream_t stream);
+
 cudaError_t launch_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose, float* out,
                                    cudaStream_t stream);
 

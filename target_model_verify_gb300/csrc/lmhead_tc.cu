@@ -434,9 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // items dealt across the grid, while the tensor cores work. The warp
       // on the MMA issuer's scheduler (warp 13) stays out of it.
       const __nv_bfloat16* dl = static_cast<const __nv_bfloat16*>(p.ep.dl);
-      const int g1 = p.gamma + 1;
-      const int n_draft = (p.M / g1) * p.gamma + min(p.M % g1, p.gamma);
-      const long long n_items = (long long)n_draft * p.ep.Pq;
+      const long long n_items = (long long)p.ep.n_qrows * p.ep.Pq;
       const int ns = gridDim.x * kQStreamWarps;
       for (long long it = (long long)blockIdx.x * kQStreamWarps + (warp - kQWarp0); it < n_items;
            it += ns) {

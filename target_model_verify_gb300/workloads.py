@@ -38,10 +38,21 @@ class Workload:
     sigma: float = 0.7               # draft noise, or the low end of U[lo, hi] per sequence
     sigma_hi: float | None = None    # set: sigma_b ~ U[sigma, sigma_hi] per sequence
     near_dup_frac: float = 0.0       # share of hidden rows replaced by a near copy of another
+    tree: tuple | None = None        # token tree (parent of every node) instead of a chain
+
+    @property
+    def N(self) -> int:
+        """Rows per sequence: gamma + 1 positions, or the tree's nodes."""
+        return len(self.tree) if self.tree is not None else self.gamma + 1
+
+    @property
+    def n_draft(self) -> int:
+        """Draft-logit rows per sequence (every tree node has one)."""
+        return len(self.tree) if self.tree is not None else self.gamma
 
     @property
     def M(self) -> int:
-        return self.B * (self.gamma + 1)
+        return self.B * self.N
 
     @property
     def elem_bytes(self) -> int:
@@ -50,9 +61,10 @@ class Workload:
     def algorithmic_bytes(self, mode: int = SAMPLE) -> int:
         """W + hidden + draft tokens (+ draft logits in sampling mode)."""
         e = self.elem_bytes
-        n = self.V * self.d * e + self.M * self.d * e + self.B * self.gamma * 4
+        n_tok = self.B * (self.N - 1 if self.tree is not None else self.gamma)
+        n = self.V * self.d * e + self.M * self.d * e + n_tok * 4
         if mode == SAMPLE:
-            n += self.B * self.gamma * self.V * e
+            n += self.B * self.n_draft * self.V * e
         return n
 
     def flops(self) -> int:
@@ -82,6 +94,15 @@ for _b in (1, 4, 16, 64, 256):
                   sigma=0.2, sigma_hi=1.5))
 _add(Workload("head_70b_b32_g7", B=32, gamma=7, d=8192, V=128256, temperature=0.7,
               w_std=0.015, sigma=0.3, sigma_hi=1.0, near_dup_frac=0.05))
+
+# A static token tree of 26 nodes, depth 5 (4, 7, 7, 5, 2 nodes per level):
+# widest near the root, where the guesses are least certain, in the manner of
+# the Medusa / EAGLE trees ("推测解码", section 不要第二个模型).
+TREE26 = (-1, 0, 0, 0, 0, 1, 1, 1, 2, 2, 3, 4, 5, 5, 6, 7, 8, 10, 11, 12, 12, 13, 14, 16, 19, 21)
+_add(Workload("llama3_8b_head_tree26", B=1, gamma=1, d=4096, V=128256, sigma=_LLAMA_SIGMA,
+              tree=TREE26))
+_add(Workload("llama3_8b_head_tree26_b8", B=8, gamma=1, d=4096, V=128256, sigma=0.2,
+              sigma_hi=1.5, tree=TREE26))
 
 
 def get(name: str, **overrides) -> Workload:
@@ -152,5 +173,57 @@ def generate(w: Workload, seed: int, device="cpu") -> dict:
         "W_lm": W.contiguous(),
         "draft_tokens": tokens.contiguous(),
         "draft_logits": draft_logits.contiguous(),
+        "sigma": sigma.float(),
+    }
+
+
+@torch.no_grad()
+def generate_tree(w: Workload, seed: int, device="cpu") -> dict:
+    """Inputs of one tree verify step, as contiguous tensors on `device`.
+
+    hidden [B, N, d], W_lm [V, d], draft_logits [B, N, V] (W (h + sigma eps)
+    at every node), node_tokens [B, N] int32 with node n's token drawn from
+    softmax(draft_logits[b, parent[n]] / T) (column 0 is 0), parent (tuple)
+    and sigma [B].
+    """
+    assert w.tree is not None
+    parent = tuple(int(x) for x in w.tree)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    dt = _torch_dtype(w)
+    B, N, d, V = w.B, len(parent), w.d, w.V
+    W = (torch.randn(V, d, generator=g, device=device) * w.w_std).to(dt)
+    h = torch.randn(B, N, d, generator=g, device=device)
+    if w.unit_rms:
+        h = h / h.pow(2).mean(dim=-1, keepdim=True).sqrt()
+    hidden = h.to(dt)
+    if w.sigma_hi is None:
+        sigma = torch.full((B,), float(w.sigma), device=device)
+    else:
+        sigma = w.sigma + (w.sigma_hi - w.sigma) * torch.rand(B, generator=g, device=device)
+    eps = torch.randn(B, N, d, generator=g, device=device)
+    rows = (hidden.float() + sigma[:, None, None] * eps).reshape(B * N, d)
+    Wf = W.float()
+    dl = torch.empty(B * N, V, dtype=dt, device=device)
+    chunk = max(1, (1 << 28) // max(V, 1))
+    for s0 in range(0, rows.shape[0], chunk):
+        dl[s0:s0 + chunk] = (rows[s0:s0 + chunk] @ Wf.T).to(dt)
+    del Wf
+    draft_logits = dl.reshape(B, N, V)
+    # Every child of a node is an independent draw from that node's q.
+    u = torch.rand(B, N, generator=g, device=device, dtype=torch.float64)
+    tokens = torch.zeros(B, N, dtype=torch.int32, device=device)
+    par = torch.tensor(parent[1:], dtype=torch.long, device=device)
+    for b in range(B if N > 1 else 0):
+        qd = torch.softmax(draft_logits[b].double() / w.temperature, dim=-1)
+        cdf = torch.cumsum(qd, dim=-1)
+        t = (u[b, 1:] * cdf[par, -1]).unsqueeze(-1)
+        tokens[b, 1:] = torch.searchsorted(cdf[par], t, right=True).squeeze(-1).clamp_max(V - 1).int()
+    return {
+        "hidden": hidden.contiguous(),
+        "W_lm": W.contiguous(),
+        "node_tokens": tokens.contiguous(),
+        "draft_logits": draft_logits.contiguous(),
+        "parent": parent,
         "sigma": sigma.float(),
     }

@@ -79,3 +79,30 @@ def test_philox_argument_errors(lib):
 def test_read_status_argument_errors(lib):
     st = ctypes.c_int32(0)
     assert lib.specdec_read_status(None, None, ctypes.byref(st)) == b.SPECDEC_ERR_INVALID_ARG
+
+
+def _tree_call(parent=(-1, 0, 0, 1), B=1, d=64, V=512, dtype=0, T=1.0, mode=0, ptr=4096, ws=256,
+               ws_bytes=1 << 30, dl=4096):
+    par = (ctypes.c_int32 * max(1, len(parent)))(*parent)
+    N = len(parent)
+    return b.specdec_verify_tree(ptr, ptr, ctypes.addressof(par), ptr, dl, B, N, d, V, dtype, T,
+                                 0, mode, ptr, ptr, ptr, ws, ws_bytes, 0)
+
+
+def test_tree_workspace_and_host_side_errors(lib):
+    n = b.specdec_verify_tree_workspace_size(2, 26, 64, 1000, 0, 0)
+    g = b.specdec_verify_tree_workspace_size(2, 26, 64, 1000, 0, 1)
+    assert n > g > 0                                   # sampling keeps logits and q records
+    assert b.specdec_verify_tree_workspace_size(2, 129, 64, 1000, 0, 0) == 0   # > max nodes
+    assert b.specdec_verify_tree_workspace_size(2, 26, 64, 1000, 1, 0) == 0    # fp32: no tree path
+    assert _tree_call(parent=(0, 0)) == b.SPECDEC_ERR_INVALID_ARG              # root not -1
+    assert _tree_call(parent=(-1, 1)) == b.SPECDEC_ERR_INVALID_ARG             # self parent
+    assert _tree_call(parent=(-1, 0, 3, 0)) == b.SPECDEC_ERR_INVALID_ARG       # later parent
+    assert _tree_call(dtype=1) == b.SPECDEC_ERR_UNSUPPORTED
+    assert _tree_call(dl=0) == b.SPECDEC_ERR_INVALID_ARG                       # sampling needs q
+    assert _tree_call(T=0.0) == b.SPECDEC_ERR_INVALID_ARG
+    assert _tree_call(ptr=4098) == b.SPECDEC_ERR_INVALID_ARG                   # 16-byte alignment
+    assert _tree_call(ws=0) == b.SPECDEC_ERR_WORKSPACE
+    assert _tree_call(ws_bytes=16) == b.SPECDEC_ERR_WORKSPACE
+    assert _tree_call(B=0) == b.SPECDEC_OK
+    assert _tree_call(mode=1, dl=0, T=0.0, ws=0) == b.SPECDEC_ERR_WORKSPACE    # greedy: no q, no T

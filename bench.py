@@ -432,9 +432,10 @@ def run_e2e(tv, w, inp, mode, K, Wm, args, device):
     ws = tv.alloc_workspace(w.B, w.gamma, w.d, w.V, inp["hidden"].dtype, mode, host=True,
                             device=device)
 
-    def step(i):
-        tv.verify_host(host["hidden"], inp["W_lm"], host["draft_tokens"], hl, w.temperature,
-                       i, mode, out_tokens=out, n_accepted=nacc, workspace=ws)
+    # The decode-loop form of the host API: bound once, then one call per
+    # step with the inputs re-read from the same pinned buffers.
+    step = tv.HostStep(host["hidden"], inp["W_lm"], host["draft_tokens"], hl, w.temperature,
+                       mode, out_tokens=out, n_accepted=nacc, workspace=ws)
 
     for i in range(Wm):
         step(i)

@@ -173,6 +173,49 @@ def verify_tree(hidden, W_lm, parent, node_tokens, draft_logits, temperature=1.0
     return out_tokens, out_nodes, n_accepted
 
 
+class HostStep:
+    """A host-I/O verify step bound once to fixed buffers, for a decode loop.
+
+    Same contract as verify_host(): hidden, draft_tokens and draft_logits
+    are pinned CPU tensors that the caller refills in place before each
+    call; out_tokens and n_accepted (pinned, allocated here if not given)
+    receive the results. The argument checks and the marshalling happen
+    once, here; each call passes only the new seed. Returns
+    (out_tokens, n_accepted) after the step's results are back on the host.
+    """
+
+    def __init__(self, hidden, W_lm, draft_tokens, draft_logits, temperature=1.0, mode=SAMPLE,
+                 out_tokens=None, n_accepted=None, workspace=None, stream=None):
+        _check_inputs(hidden, W_lm, draft_tokens, draft_logits, mode, "host")
+        if not W_lm.is_cuda or hidden.is_cuda:
+            raise ValueError("HostStep takes W_lm on the device and the step's tensors on the host")
+        B, gamma, d, V = _shape(hidden, W_lm)
+        if out_tokens is None:
+            out_tokens = torch.empty(B, gamma + 1, dtype=torch.int32, pin_memory=True)
+        if n_accepted is None:
+            n_accepted = torch.empty(B, dtype=torch.int32, pin_memory=True)
+        if workspace is None:
+            workspace = alloc_workspace(B, gamma, d, V, hidden.dtype, mode, host=True,
+                                        device=W_lm.device)
+        # keep every buffer alive for the lifetime of the step
+        self._keep = (hidden, W_lm, draft_tokens, draft_logits, workspace)
+        self.out_tokens, self.n_accepted = out_tokens, n_accepted
+        self._fn = _b.lib().specdec_verify_host
+        a = _b._SIGNATURES["specdec_verify_host"][1]
+        vals = [_ptr(hidden), _ptr(W_lm), _ptr(draft_tokens), _ptr(draft_logits), B, gamma, d, V,
+                _DTYPES[hidden.dtype], float(temperature), 0, int(mode), _ptr(out_tokens),
+                _ptr(n_accepted), _ptr(workspace), workspace.numel(), _stream_ptr(stream)]
+        self._args = [t(v) for t, v in zip(a, vals)]
+        self._seed = self._args[10]
+
+    def __call__(self, seed):
+        self._seed.value = int(seed) & (2 ** 64 - 1)
+        rc = self._fn(*self._args)
+        if rc != 0:
+            _b._check(rc, "specdec_verify_host")
+        return self.out_tokens, self.n_accepted
+
+
 def read_status(workspace, stream=None) -> int:
     """The device status word of the last call that used `workspace`."""
     return _b.specdec_read_status(_ptr(workspace), _stream_ptr(stream))

@@ -58,6 +58,9 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--loop-c", type=float, default=None,
+                    help="time the draft->verify loop with a synthetic drafter costing this "
+                         "fraction of a target step per draft token (prints its own line)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -499,11 +502,106 @@ def run_reference(args, world, rank, local):
     print(json.dumps(line), flush=True)
 
 
+def run_loop(args):
+    """The draft -> verify loop on one GPU, against its closed form.
+
+    "推测解码", section 快多少: with acceptance rate alpha, gamma guesses per
+    step and a draft step costing c target steps, a step costs gamma*c + 1
+    target steps and writes (1 - alpha^(gamma+1)) / (1 - alpha) tokens on
+    average. Here every position has the same p and q (one hidden row and
+    one draft-logit row repeated), so acceptances are independent with alpha
+    = sum_v min(p, q); the drafter is a GPU busy-wait of c target steps per
+    guess, its guesses fresh draws from q every step; the target step is the
+    LM head scoring one position (a greedy verify of one guess reads W once).
+    """
+    import target_model_verify_gb300 as tv
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = wl.get(args.workload)
+    if w.tree is not None:
+        raise SystemExit("--loop-c runs the chain step")
+    B, gamma, d, V, T = w.B, w.gamma, w.d, w.V, w.temperature
+    base = wl.generate(w, args.seed, device=device)
+    W = base["W_lm"]
+    hidden = base["hidden"][:, :1].expand(B, gamma + 1, d).contiguous()
+    dl = base["draft_logits"][:, :1].expand(B, gamma, V).contiguous()
+    p = torch.softmax((hidden[:, 0].float() @ W.float().T) / T, dim=-1)
+    q = torch.softmax(dl[:, 0].float() / T, dim=-1)
+    alpha = float(torch.minimum(p, q).sum(dim=-1).mean())
+    K, Wm = args.steps, args.warmup
+    g = torch.Generator(device=device)
+    g.manual_seed(args.seed + 17)
+    draws = torch.multinomial(q, (K + Wm) * gamma, replacement=True, generator=g)
+    drafts = draws.view(B, K + Wm, gamma).transpose(0, 1).contiguous().int()
+    ws = tv.alloc_workspace(B, gamma, d, V, W.dtype, wl.SAMPLE, device=device)
+    out = torch.empty(B, gamma + 1, dtype=torch.int32, device=device)
+    naccs = torch.empty(K + Wm, B, dtype=torch.int32, device=device)
+
+    def timed(fn, n):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        for i in range(3):
+            fn(i)
+        torch.cuda.synchronize()
+        e0.record()
+        for i in range(n):
+            fn(i)
+        e1.record()
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    # one target step: the LM head reading W once for one position per sequence
+    h1 = hidden[:, :2].contiguous()
+    ws1 = tv.alloc_workspace(B, 1, d, V, W.dtype, wl.GREEDY, device=device)
+    t_target = timed(lambda i: tv.verify(h1, W, drafts[0][:, :1].contiguous(), None, T, i,
+                                         wl.GREEDY, workspace=ws1), 300)
+    # the drafter: a busy-wait calibrated in SM cycles
+    calib = 2_000_000
+    us_per_cycle = timed(lambda i: torch.cuda._sleep(calib), 20) / calib
+    draft_cycles = max(1, int(args.loop_c * t_target / us_per_cycle))
+    t_draft = timed(lambda i: torch.cuda._sleep(draft_cycles), 200)
+
+    def step(i):
+        for _ in range(gamma):
+            torch.cuda._sleep(draft_cycles)
+        tv.verify(hidden, W, drafts[i], dl, T, args.seed * 1_000_003 + i, wl.SAMPLE,
+                  out_tokens=out, n_accepted=naccs[i], workspace=ws)
+
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for k in range(K):
+        step(Wm + k)
+    e1.record()
+    torch.cuda.synchronize()
+    t_step = e0.elapsed_time(e1) * 1e3 / K
+    tokens = float((naccs[Wm:].double() + 1).mean())
+    c_eff = t_draft / t_target
+    tok_closed = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+    line = {
+        "metric": "speculative decoding speed-up over one token per target step (draft->verify loop)",
+        "value": tokens * t_target / t_step,
+        "unit": "x",
+        "closed_form": tok_closed / (gamma * c_eff + 1),
+        "closed_form_with_verify_cost": tok_closed / (gamma * c_eff + (t_step - gamma * t_draft) / t_target),
+        "alpha": alpha, "gamma": gamma, "c": c_eff, "steps": K, "warmup": Wm,
+        "tokens_per_step": tokens, "closed_form_tokens_per_step": tok_closed,
+        "target_step_us": t_target, "draft_token_us": t_draft, "loop_step_us": t_step,
+        "verify_us": t_step - gamma * t_draft,
+        "config": {"workload": args.workload, "B": B, "d": d, "V": V, "temperature": T},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
     if args.gpus != world and world > 1:
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
+    if args.loop_c is not None:
+        run_loop(args)
+        return
     if args.impl == "reference":
         run_reference(args, world, rank, local)
     else:

@@ -206,6 +206,58 @@ def test_host_entry_point_matches_device_entry_point():
     np.testing.assert_array_equal(nacc.numpy(), dev_nacc)
 
 
+def test_prepared_host_step_rereads_its_buffers_each_call():
+    """HostStep: bound once; each call re-reads the pinned inputs the caller
+    refilled and matches the device entry point for that input and seed."""
+    import target_model_verify_gb300 as tv
+    w, inp0 = _gen("llama3_8b_head", 6, B=3, V=4000, d=256)
+    _, inp1 = _gen("llama3_8b_head", 7, B=3, V=4000, d=256)
+    inp1["W_lm"] = inp0["W_lm"]
+    host = {k: v.cpu().pin_memory() for k, v in inp0.items() if k not in ("W_lm", "sigma")}
+    step = tv.HostStep(host["hidden"], inp0["W_lm"], host["draft_tokens"], host["draft_logits"],
+                       1.0, ov.SAMPLE)
+    for seed, inp in ((8, inp0), (9, inp1), (8, inp0)):
+        for k in host:
+            host[k].copy_(inp[k].cpu())
+        out, nacc = step(seed)
+        dev_out, dev_nacc, _ = parity.run_library(inp, 1.0, seed, ov.SAMPLE, debug=False)
+        np.testing.assert_array_equal(out.numpy(), dev_out)
+        np.testing.assert_array_equal(nacc.numpy(), dev_nacc)
+
+
+def test_tokens_per_step_match_the_closed_form():
+    """Independent positions with one p and one q everywhere: the number of
+    drafts kept follows P(j = k) = alpha^k (1 - alpha) (k < gamma), alpha^gamma
+    (k = gamma), so the tokens written per step average (1 - alpha^(gamma+1))
+    / (1 - alpha) ("推测解码", section 接受率 α), alpha = sum_v min(p, q)."""
+    import target_model_verify_gb300 as tv
+    V, d, B, gamma = 64, 64, 20000, 4
+    w = wl.get("llama3_8b_head", B=1, gamma=gamma, d=d, V=V, sigma=0.8, w_std=0.3)
+    base = wl.generate(w, 5, device=DEV)
+    hidden = base["hidden"][:, :1].expand(B, gamma + 1, d).contiguous()
+    dl = base["draft_logits"][:, :1].expand(B, gamma, V).contiguous()
+    one = {"hidden": base["hidden"][:, :2].contiguous(), "W_lm": base["W_lm"],
+           "draft_tokens": base["draft_tokens"][:, :1].contiguous(),
+           "draft_logits": base["draft_logits"][:, :1].contiguous()}
+    res = parity.run_oracle(one, 1.0, 0, ov.SAMPLE)
+    p = ov.softmax_t(res.z[0, 0], 1.0)[0]
+    q = ov.softmax_t(parity.to_f64(base["draft_logits"][0, 0]), 1.0)[0]
+    alpha = float(np.minimum(p, q).sum())
+    g = torch.Generator(device=DEV)
+    g.manual_seed(3)
+    x = torch.multinomial(torch.as_tensor(q, device=DEV).float(), B * gamma, replacement=True,
+                          generator=g).view(B, gamma).int()
+    _, nacc = tv.verify(hidden, base["W_lm"], x, dl, 1.0, 77, ov.SAMPLE)
+    n = (nacc.double() + 1).cpu().numpy()
+    pk = np.array([alpha ** k * (1 - alpha) for k in range(gamma)] + [alpha ** gamma])
+    vals = np.arange(1, gamma + 2)
+    mean, var = float((pk * vals).sum()), float((pk * vals ** 2).sum() - (pk * vals).sum() ** 2)
+    assert abs(mean - (1 - alpha ** (gamma + 1)) / (1 - alpha)) < 1e-12
+    assert abs(n.mean() - mean) < 5 * np.sqrt(var / B), (n.mean(), mean, alpha)
+    counts = np.bincount(n.astype(int) - 1, minlength=gamma + 1)
+    assert np.all(np.abs(counts / B - pk) < 5 * np.sqrt(pk * (1 - pk) / B) + 1e-12)
+
+
 def test_chi_square_committed_token_law():
     """Distribution preservation on the GPU: over 2*10^5 draws the first
     written token follows p0 and the kept fraction is sum min(p0, q0)

@@ -15,7 +15,7 @@
 namespace specdec {
 namespace {
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 512;   // one warp per record row: up to 2*32+1 rows in one round
 constexpr int kBatch = 8;
 
 template <typename DL>
@@ -33,6 +33,20 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
 
   grid_dependency_wait();      // the LM-head kernel's records are complete
   grid_launch_dependents();    // the sampler may start launching
+
+  // The drafted tokens' logits do not depend on the folds: warp 0 loads
+  // them first, so their latency overlaps the record loads.
+  __shared__ float s_zx[SPECDEC_MAX_GAMMA], s_zqx[SPECDEC_MAX_GAMMA];
+  __shared__ int s_x[SPECDEC_MAX_GAMMA];
+  if (warp == 0 && lane < gamma) {
+    const int x = a.draft_tokens[b * gamma + lane];
+    s_x[lane] = x;
+    if (sample && x >= 0 && x < a.V) {
+      const DL* dl = static_cast<const DL*>(a.dl);
+      s_zx[lane] = a.z[(size_t)(b * g1 + lane) * a.V + x];
+      s_zqx[lane] = load_logit(dl, ((size_t)b * gamma + lane) * a.V + x);
+    }
+  }
 
   for (int r = warp; r < rows; r += kThreads / 32) {
     float m = -INFINITY, s = 0.f;
@@ -103,15 +117,14 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
   bool bad = false, rej = false;
   int x = -1;
   if (lane < gamma) {
-    x = a.draft_tokens[b * gamma + lane];
+    x = s_x[lane];
     if (x < 0 || x >= a.V) {
       bad = true;
     } else if (!sample) {
       rej = x != s_ai[lane];
     } else {
-      const DL* dl = static_cast<const DL*>(a.dl);
-      const float zx = a.z[(size_t)(b * g1 + lane) * a.V + x];
-      const float zqx = load_logit(dl, ((size_t)b * gamma + lane) * a.V + x);
+      const float zx = s_zx[lane];
+      const float zqx = s_zqx[lane];
       const float px = exp2f((zx - s_pm[lane]) * a.c - log2f(s_ps[lane]));
       const float qx = exp2f((zqx - s_qm[lane]) * a.c - log2f(s_qs[lane]));
       const float r = accept_uniform(a.seed, b, lane);

@@ -380,6 +380,11 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t smem, in
       "r"(smem), "r"(x), "r"(y)
       : "memory");
 }
+// Bulk prefetch of [addr, addr + bytes) into L2 (16-byte aligned, bytes a
+// multiple of 16).
+__device__ __forceinline__ void bulk_prefetch_l2(const void* addr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(addr), "r"(bytes) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

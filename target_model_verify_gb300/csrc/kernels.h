@@ -61,6 +61,7 @@ cudaError_t launch_accept(const AcceptLaunch& L, cudaStream_t stream);
 struct SampleLaunch {
   int B, gamma, V, nchunks, dl_bf16;
   int vec;          // set by the launcher: 16-byte logit and draft-logit loads are aligned
+  int prefetch;     // set by the launcher: small batch, rows prefetched into L2 early
   float c;
   uint64_t seed;
   const float* z;

@@ -147,6 +147,21 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
 
   const int b = blockIdx.y;
   const int chunk = blockIdx.x;
+  if (L.prefetch && threadIdx.x < 2 * (L.gamma + 1)) {
+    // Small batch: the row is not known yet, but every candidate row's chunk
+    // was written by the LM-head kernel, which finished before the
+    // acceptance kernel began; pull them into L2 while that kernel runs.
+    const int r = threadIdx.x >> 1;
+    const int v0 = chunk * kChunkV;
+    const int n = min(kChunkV, L.V - v0);
+    if (threadIdx.x & 1) {
+      if (r < L.gamma)
+        bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(L.dl) + ((size_t)b * L.gamma + r) * L.V + v0,
+                         (uint32_t)n * 2u);
+    } else {
+      bulk_prefetch_l2(L.z + ((size_t)b * (L.gamma + 1) + r) * L.V + v0, (uint32_t)n * 4u);
+    }
+  }
   grid_dependency_wait();      // the acceptance kernel's selection is complete
   const SelectedRow sr = L.sel[b];
   if (sr.j < 0) return;
@@ -260,6 +275,12 @@ cudaError_t launch_sample(const SampleLaunch& L0, cudaStream_t stream) {
            ((uintptr_t)L.dl & (dl_align - 1)) == 0)
               ? 1
               : 0;
+  // Bulk prefetches need 16-byte aligned rows of both arrays (bf16 draft
+  // logits: V % 8 == 0); only worth it while the rows are few.
+  L.prefetch = (L.dl_bf16 && L.B <= 16 && L.V % 8 == 0 && ((uintptr_t)L.z & 15u) == 0 &&
+                ((uintptr_t)L.dl & 15u) == 0)
+                   ? 1
+                   : 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.nchunks, L.B);
   cfg.blockDim = dim3(kSampleThreads);

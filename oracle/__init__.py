@@ -19,11 +19,15 @@ What it computes, and where the pages fix it:
 * ``tree``     -- tree verification: the same rule at every fork of a token
   tree (siblings in order, the residual renormalised after each rejection),
   "推测解码", section 不要第二个模型; a chain-shaped tree is the chain step.
+* ``attention`` -- verify-step attention: the gamma + 1 new positions of a
+  sequence over its KV cache, causal among themselves, grouped-query heads
+  ("推测解码", section 几段话一起写: every sequence reads its own cache).
 * ``formulas`` -- the closed forms the same page prints: tokens per weight
   read, speedup, arithmetic overhead (sections 接受率 α, 快多少,
   用的是闲着的算术).
 
-Pins (tests/test_oracle_pins.py, tests/test_oracle_tree_pins.py) tie every
+Pins (tests/test_oracle_pins.py, tests/test_oracle_tree_pins.py,
+tests/test_oracle_attention_pins.py) tie every
 function to something other than itself: a library Philox (triton's
 interpreter), brute-force loops, exact enumeration over all 2^24 uniform
 values, exact rational enumeration of the tree rule's output law, chi-square

@@ -58,6 +58,9 @@ def parse_args(argv=None):
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--attention", default=None, metavar="B,L,N",
+                    help="time verify-step attention for one Llama-3-8B-shaped layer (32 query, "
+                         "8 KV heads, D 128): B sequences of L cached tokens, N new positions")
     ap.add_argument("--loop-c", type=float, default=None,
                     help="time the draft->verify loop with a synthetic drafter costing this "
                          "fraction of a target step per draft token (prints its own line)")
@@ -594,6 +597,62 @@ def run_loop(args):
     print(json.dumps(line), flush=True)
 
 
+def run_attention(args):
+    """Verify-step attention for one layer: one GPU, CUDA events, inputs far
+    larger than L2 ("推测解码", section 几段话一起写: every sequence reads its
+    own KV cache, 131 KB per token over Llama 3.1 8B's 32 layers)."""
+    import target_model_verify_gb300 as tv
+    B, L, n_new = (int(x) for x in args.attention.split(","))
+    Hq, Hkv, D = 32, 8, 128
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(args.seed)
+    q = torch.randn(B, n_new, Hq, D, generator=g, device=device).to(torch.bfloat16)
+    k = torch.randn(B, L, Hkv, D, generator=g, device=device).to(torch.bfloat16)
+    v = torch.randn(B, L, Hkv, D, generator=g, device=device).to(torch.bfloat16)
+    lens = torch.full((B,), L, dtype=torch.int32, device=device)
+    out = torch.empty(B, n_new, Hq, D, dtype=torch.float32, device=device)
+    ws = torch.empty(tv.attention_workspace_bytes(B, n_new, Hq, Hkv, D, L), dtype=torch.uint8,
+                     device=device)
+    K, Wm = args.steps, args.warmup
+    for _ in range(Wm):
+        tv.verify_attention(q, k, v, lens, out=out, workspace=ws)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(0)
+    time.sleep(0.6)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t_wall0 = time.time()
+    e0.record()
+    for _ in range(K):
+        tv.verify_attention(q, k, v, lens, out=out, workspace=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    time.sleep(0.2)
+    sampler.stop()
+    if tv.read_status(ws) != 0:
+        raise RuntimeError("device status after attention")
+    us = e0.elapsed_time(e1) * 1e3 / K
+    kv_bytes = 2 * B * L * Hkv * D * 2
+    bytes_alg = kv_bytes + q.numel() * 2 + out.numel() * 4
+    peaks, kind = load_peaks()
+    achieved = bytes_alg / (us * 1e-6) / 1e9
+    line = {
+        "metric": "verify-step attention, one Llama-3-8B-shaped layer", "value": us,
+        "unit": "us", "higher_is_better": False, "steps": K, "warmup": Wm,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "algorithmic_bytes": bytes_alg, "kernel": "attn_split_kernel",
+                     "peak_source": f"{kind} (MEASURED_PEAKS.json)"},
+        "config": {"B": B, "cached_tokens": L, "new_positions": n_new, "Hq": Hq, "Hkv": Hkv,
+                   "D": D, "l2": "KV cache larger than L2 per call" if kv_bytes > 129e6 else
+                   "KV cache smaller than L2"},
+        "clocks": sampler.summary(t_wall0, t_wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
@@ -601,6 +660,9 @@ def main(argv=None):
         raise SystemExit(f"--gpus {args.gpus} but WORLD_SIZE={world}")
     if args.loop_c is not None:
         run_loop(args)
+        return
+    if args.attention is not None:
+        run_attention(args)
         return
     if args.impl == "reference":
         run_reference(args, world, rank, local)

@@ -225,6 +225,31 @@ int specdec_verify_tree_timed(const void* hidden, const void* W_lm, const int32_
                               void* stream, void* lmhead_start_event, void* lmhead_end_event);
 
 /*
+ * Verify-step attention for one layer ("推测解码", section 几段话一起写:
+ * every sequence reads its own KV cache each step). The n_new = gamma + 1
+ * new positions of every sequence attend to their causal window of the
+ * sequence's cache:
+ *   q        [B, n_new, Hq, D]   bf16   queries of the new positions
+ *   k_cache  [B, Lmax, Hkv, D]   bf16   keys; rows < seq_lens[b] are valid and
+ *   v_cache  [B, Lmax, Hkv, D]   bf16   the last n_new of them are the new positions
+ *   seq_lens [B]                 int32  (device) valid rows, n_new <= L <= Lmax;
+ *                                       otherwise the status word gets
+ *                                       SPECDEC_ERR_INVALID_ARG and that
+ *                                       sequence's output is 0
+ *   out      [B, n_new, Hq, D]   fp32   o = sum_j softmax_j(scale q.k_j) v_j over
+ *                                       rows j <= seq_len - n_new + i
+ * Query head h reads KV head h / (Hq / Hkv). scale <= 0 selects 1/sqrt(D).
+ * Limits: D = 128, Hq % Hkv == 0, n_new * Hq / Hkv <= 64, B >= 0 (0 is a
+ * no-op), Lmax >= n_new; q, caches and out 16-byte aligned. The status word
+ * sits at the start of the workspace (specdec_read_status). Asynchronous.
+ */
+size_t specdec_verify_attention_workspace_size(int B, int n_new, int Hq, int Hkv, int D, int Lmax);
+int specdec_verify_attention(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* seq_lens, int B, int n_new, int Hq, int Hkv, int D,
+                             int Lmax, float scale, float* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/*
  * Reads the device status word of a workspace after synchronising `stream`:
  * SPECDEC_OK, SPECDEC_ERR_TIMEOUT or SPECDEC_ERR_TOKEN_RANGE of the last
  * call that used it. *status receives the value; the return code reports

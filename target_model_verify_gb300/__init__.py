@@ -173,6 +173,38 @@ def verify_tree(hidden, W_lm, parent, node_tokens, draft_logits, temperature=1.0
     return out_tokens, out_nodes, n_accepted
 
 
+def attention_workspace_bytes(B, n_new, Hq, Hkv, D, Lmax) -> int:
+    return _b.specdec_verify_attention_workspace_size(B, n_new, Hq, Hkv, D, Lmax)
+
+
+def verify_attention(q, k_cache, v_cache, seq_lens, scale=0.0, out=None, workspace=None,
+                     stream=None):
+    """Verify-step attention for one layer (include/specdec_verify.h).
+
+    q [B, n_new, Hq, D], k_cache / v_cache [B, Lmax, Hkv, D] (bf16, CUDA),
+    seq_lens [B] int32 (CUDA). Returns out [B, n_new, Hq, D] fp32.
+    """
+    for t in (q, k_cache, v_cache):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("q and the caches must be contiguous bfloat16 CUDA tensors")
+    if seq_lens.dtype != torch.int32 or not seq_lens.is_cuda:
+        raise TypeError("seq_lens must be an int32 CUDA tensor")
+    B, n_new, Hq, D = q.shape
+    Lmax, Hkv = k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty(B, n_new, Hq, D, dtype=torch.float32, device=q.device)
+    if workspace is None:
+        n = attention_workspace_bytes(B, n_new, Hq, Hkv, D, Lmax)
+        if n == 0:
+            raise SpecdecError(_b.SPECDEC_ERR_UNSUPPORTED, "attention_workspace_bytes")
+        workspace = torch.empty(n, dtype=torch.uint8, device=q.device)
+    rc = _b.specdec_verify_attention(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(seq_lens), B,
+                                     n_new, Hq, Hkv, D, Lmax, float(scale), _ptr(out),
+                                     _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _b._check(rc, "specdec_verify_attention")
+    return out
+
+
 class HostStep:
     """A host-I/O verify step bound once to fixed buffers, for a decode loop.
 

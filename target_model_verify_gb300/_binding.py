@@ -56,6 +56,9 @@ _SIGNATURES = {
     "specdec_verify_tree_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "specdec_verify_tree": (_i, _TREE),
     "specdec_verify_tree_timed": (_i, _TREE + [_vp, _vp]),
+    "specdec_verify_attention_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "specdec_verify_attention": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp,
+                                      _sz, _vp]),
 }
 
 _lib = None
@@ -143,6 +146,14 @@ def specdec_verify_tree(*args) -> int:
 
 def specdec_verify_tree_timed(*args) -> int:
     return int(lib().specdec_verify_tree_timed(*args))
+
+
+def specdec_verify_attention_workspace_size(B, n_new, Hq, Hkv, D, Lmax) -> int:
+    return int(lib().specdec_verify_attention_workspace_size(B, n_new, Hq, Hkv, D, Lmax))
+
+
+def specdec_verify_attention(*args) -> int:
+    return int(lib().specdec_verify_attention(*args))
 
 
 def specdec_read_status(workspace_ptr: int, stream_ptr: int) -> int:

@@ -360,6 +360,50 @@ TreePlan make_tree_plan(int B, int N, int d, int V, int mode) {
   return p;
 }
 
+// ----------------------------------------------------------- attention --
+
+struct AttnPlan {
+  int n_splits, split_len;
+  size_t off_m, off_l, off_o, total;
+};
+
+int check_attn_shape(int B, int n_new, int Hq, int Hkv, int D, int Lmax) {
+  if (B < 0 || n_new < 1 || Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || D != 128 || Lmax < n_new)
+    return SPECDEC_ERR_UNSUPPORTED;
+  if ((long long)n_new * (Hq / Hkv) > 64) return SPECDEC_ERR_UNSUPPORTED;
+  if ((long long)B * Lmax * Hkv * D >= (1ll << 40)) return SPECDEC_ERR_UNSUPPORTED;
+  return SPECDEC_OK;
+}
+
+// Splits of the key range: none once the (sequence, KV head) pairs alone
+// fill two waves of a 152-SM part; otherwise enough for four waves, at least
+// 256 keys each (fixed targets, so the workspace size does not depend on
+// the device).
+AttnPlan make_attn_plan(int B, int n_new, int Hq, int Hkv, int Lmax) {
+  AttnPlan p;
+  const long long pairs = (long long)B * Hkv;
+  long long want = pairs >= 304 ? 1 : pairs > 0 ? (608 + pairs - 1) / pairs : 1;
+  const long long most = (Lmax + 255) / 256;
+  if (want > most) want = most;
+  if (want < 1) want = 1;
+  int split = (int)((Lmax + want - 1) / want);
+  split = (split + 63) / 64 * 64;
+  p.split_len = split;
+  p.n_splits = (Lmax + split - 1) / split;
+  size_t off = align_up(sizeof(WsHeader));
+  const size_t rows = (size_t)B * Hkv * p.n_splits * 64;
+  p.off_m = off;
+  p.off_l = off;
+  p.off_o = off;
+  if (p.n_splits > 1) {
+    p.off_l = align_up(off + sizeof(float) * rows);
+    p.off_o = align_up(p.off_l + sizeof(float) * rows);
+    off = align_up(p.off_o + sizeof(float) * rows * 128);
+  }
+  p.total = off;
+  return p;
+}
+
 }  // namespace
 
 namespace specdec {
@@ -643,6 +687,50 @@ int specdec_verify_tree(const void* hidden, const void* W_lm, const int32_t* par
                                    V, dtype, temperature, seed, mode, out_tokens, out_nodes,
                                    n_accepted, workspace, workspace_bytes, stream, nullptr,
                                    nullptr);
+}
+
+size_t specdec_verify_attention_workspace_size(int B, int n_new, int Hq, int Hkv, int D,
+                                               int Lmax) {
+  if (check_attn_shape(B, n_new, Hq, Hkv, D, Lmax) != SPECDEC_OK) return 0;
+  return make_attn_plan(B, n_new, Hq, Hkv, Lmax).total;
+}
+
+int specdec_verify_attention(const void* q, const void* k_cache, const void* v_cache,
+                             const int32_t* seq_lens, int B, int n_new, int Hq, int Hkv, int D,
+                             int Lmax, float scale, float* out, void* workspace,
+                             size_t workspace_bytes, void* stream_ptr) {
+  int rc = check_attn_shape(B, n_new, Hq, Hkv, D, Lmax);
+  if (rc != SPECDEC_OK) return rc;
+  if (B == 0) return SPECDEC_OK;
+  if (!q || !k_cache || !v_cache || !seq_lens || !out) return SPECDEC_ERR_INVALID_ARG;
+  if ((((uintptr_t)q | (uintptr_t)k_cache | (uintptr_t)v_cache | (uintptr_t)out) & 15u) != 0)
+    return SPECDEC_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return SPECDEC_ERR_INVALID_ARG;
+  const AttnPlan pl = make_attn_plan(B, n_new, Hq, Hkv, Lmax);
+  if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || workspace_bytes < pl.total)
+    return SPECDEC_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  AttnLaunch A;
+  A.B = B;
+  A.n_new = n_new;
+  A.Hq = Hq;
+  A.Hkv = Hkv;
+  A.Lmax = Lmax;
+  A.n_splits = pl.n_splits;
+  A.split_len = pl.split_len;
+  A.scale_log2 = (scale > 0.f ? scale : 1.f / std::sqrt((float)D)) * kLog2e;
+  A.q = static_cast<const __nv_bfloat16*>(q);
+  A.k = static_cast<const __nv_bfloat16*>(k_cache);
+  A.v = static_cast<const __nv_bfloat16*>(v_cache);
+  A.seq_lens = seq_lens;
+  A.out = out;
+  A.part_m = reinterpret_cast<float*>(ws + pl.off_m);
+  A.part_l = reinterpret_cast<float*>(ws + pl.off_l);
+  A.part_o = reinterpret_cast<float*>(ws + pl.off_o);
+  A.status = reinterpret_cast<int*>(ws);
+  return launch_attention(A, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
 int specdec_read_status(const void* workspace, void* stream, int32_t* status) {

@@ -95,6 +95,23 @@ struct TreeLaunch {
 };
 cudaError_t launch_tree_walk(const TreeLaunch& L, cudaStream_t stream);
 
+// Verify-step attention (one layer): split-KV partials and their merge.
+struct AttnLaunch {
+  int B, n_new, Hq, Hkv, Lmax, n_splits, split_len;
+  float scale_log2;                  // softmax scale times log2(e)
+  const __nv_bfloat16* q;            // [B, n_new, Hq, 128]
+  const __nv_bfloat16* k;            // [B, Lmax, Hkv, 128]
+  const __nv_bfloat16* v;
+  const int32_t* seq_lens;           // [B]
+  float* out;                        // [B, n_new, Hq, 128]
+  float* part_m;                     // [B, Hkv, n_splits, 64] (n_splits > 1)
+  float* part_l;
+  float* part_o;                     // [B, Hkv, n_splits, 64, 128]
+  int* status;
+};
+cudaError_t launch_attention(const AttnLaunch& A, cudaStream_t stream);
+int attn_smem_bytes();
+
 cudaError_t launch_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose, float* out,
                                    cudaStream_t stream);
 

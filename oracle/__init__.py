@@ -22,12 +22,16 @@ What it computes, and where the pages fix it:
 * ``attention`` -- verify-step attention: the gamma + 1 new positions of a
   sequence over its KV cache, causal among themselves, grouped-query heads
   ("推测解码", section 几段话一起写: every sequence reads its own cache).
+* ``cluster_head`` -- the drafter's clustered LM head: cluster logits, the
+  top-k clusters, token logits of their members only, the draft token
+  ("多詞元預測視覺化指南", section 高效嵌入器).
 * ``formulas`` -- the closed forms the same page prints: tokens per weight
   read, speedup, arithmetic overhead (sections 接受率 α, 快多少,
   用的是闲着的算术).
 
 Pins (tests/test_oracle_pins.py, tests/test_oracle_tree_pins.py,
-tests/test_oracle_attention_pins.py) tie every
+tests/test_oracle_attention_pins.py, tests/test_oracle_cluster_pins.py) tie
+every
 function to something other than itself: a library Philox (triton's
 interpreter), brute-force loops, exact enumeration over all 2^24 uniform
 values, exact rational enumeration of the tree rule's output law, chi-square

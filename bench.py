@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--attention", default=None, metavar="B,L,N",
                     help="time verify-step attention for one Llama-3-8B-shaped layer (32 query, "
                          "8 KV heads, D 128): B sequences of L cached tokens, N new positions")
+    ap.add_argument("--cluster-head", default=None, metavar="M,K",
+                    help="time the drafter's clustered LM head at the Gemma-E2B shape "
+                         "(V 262144, d 1536, 2048 clusters of 128): M rows, K kept clusters")
     ap.add_argument("--loop-c", type=float, default=None,
                     help="time the draft->verify loop with a synthetic drafter costing this "
                          "fraction of a target step per draft token (prints its own line)")
@@ -597,6 +600,53 @@ def run_loop(args):
     print(json.dumps(line), flush=True)
 
 
+def run_cluster_head(args):
+    """The drafter's clustered LM head ("多詞元預測視覺化指南", section
+    高效嵌入器): cluster logits, the top-K clusters, their members' logits and
+    the draft token, against the bytes of the full head."""
+    import target_model_verify_gb300 as tv
+    M, K = (int(x) for x in args.cluster_head.split(","))
+    V, d, n_c = 262144, 1536, 2048
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(args.seed)
+    W = (torch.randn(V, d, generator=g, device=device) * 0.02).to(torch.bfloat16)
+    size = V // n_c
+    E = W.view(n_c, size, d).float().mean(1).to(torch.bfloat16)
+    starts = torch.arange(0, V + 1, size, dtype=torch.int32, device=device)
+    tor = torch.randperm(V, generator=g, device=device).int()
+    h = torch.randn(M, d, generator=g, device=device)
+    h = (h / h.pow(2).mean(-1, keepdim=True).sqrt() * 3.0).to(torch.bfloat16)
+    ws = torch.empty(tv._b.specdec_cluster_head_workspace_size(M, n_c, K, size), dtype=torch.uint8,
+                     device=device)
+    step = lambda i: tv.cluster_head(h, E, W, starts, tor, top_k=K, max_cluster=size, seed=i,
+                                     position=i, workspace=ws)
+    Kst, Wm = args.steps, args.warmup
+    for i in range(Wm):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(Kst):
+        step(Wm + i)
+    e1.record()
+    torch.cuda.synchronize()
+    if tv.read_status(ws) != 0:
+        raise RuntimeError("device status after the clustered head")
+    us = e0.elapsed_time(e1) * 1e3 / Kst
+    bytes_read = n_c * d * 2 + M * K * size * d * 2 + M * d * 2
+    line = {
+        "metric": "drafter clustered LM head, one call", "value": us, "unit": "us",
+        "higher_is_better": False, "steps": Kst, "warmup": Wm,
+        "bytes_read": bytes_read, "full_head_bytes": V * d * 2,
+        "achieved_gbs": bytes_read / (us * 1e-6) / 1e9,
+        "config": {"M": M, "top_k": K, "V": V, "d": d, "clusters": n_c, "cluster_size": size,
+                   "mode": "sample", "l2": "cluster table and kept rows fit in L2 (latency-bound)"},
+    }
+    print(json.dumps(line), flush=True)
+
+
 def run_attention(args):
     """Verify-step attention for one layer: one GPU, CUDA events, inputs far
     larger than L2 ("推测解码", section 几段话一起写: every sequence reads its
@@ -663,6 +713,9 @@ def main(argv=None):
         return
     if args.attention is not None:
         run_attention(args)
+        return
+    if args.cluster_head is not None:
+        run_cluster_head(args)
         return
     if args.impl == "reference":
         run_reference(args, world, rank, local)

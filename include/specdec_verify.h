@@ -250,6 +250,41 @@ int specdec_verify_attention(const void* q, const void* k_cache, const void* v_c
                              size_t workspace_bytes, void* stream);
 
 /*
+ * The drafter's clustered LM head ("多詞元預測視覺化指南", section 高效嵌入器):
+ * cluster logits y = h E^T, the top_k clusters of every row (largest y, ties
+ * to the lower index), token logits z = h . W_r for the kept clusters'
+ * member rows only, and the draft token: greedy, the argmax of z (lowest
+ * token ID on ties); sampling, the smallest token ID whose prefix sum (in
+ * token-ID order) of exp((z - max z) / T) passes u * S, with u from Philox
+ * counter (row m, position, purpose 2).
+ *   hidden        [M, d]       bf16   drafter hidden states, M <= 64
+ *   cluster_emb   [n_c, d]     bf16   one embedding per cluster
+ *   W_sorted      [V, d]       bf16   token embeddings grouped by cluster
+ *   starts        [n_c + 1]    int32  (device) cluster c owns rows starts[c] ..
+ *                                     starts[c+1] - 1 of W_sorted
+ *   token_of_row  [V]          int32  (device) token ID of every W_sorted row
+ *   max_cluster   host bound on any cluster's size; a kept cluster above it
+ *                 sets SPECDEC_ERR_INVALID_ARG in the status word
+ *   out_tokens    [M] int32, out_clusters [M, top_k] int32 (best first)
+ *   logits_out    [M, V] fp32 or NULL: the kept tokens' logits are written
+ *                 there (other entries are left as the caller set them)
+ * Limits: 1 <= top_k <= SPECDEC_CLUSTER_MAX_TOP_K, d % 8 == 0,
+ * d <= SPECDEC_CLUSTER_MAX_D, top_k * max_cluster <=
+ * SPECDEC_CLUSTER_MAX_MEMBERS, top_k <= n_c; bf16 pointers 16-byte aligned.
+ * Asynchronous; status word at the start of the workspace.
+ */
+#define SPECDEC_CLUSTER_MAX_TOP_K 8
+#define SPECDEC_CLUSTER_MAX_D 4096
+#define SPECDEC_CLUSTER_MAX_MEMBERS 4096
+size_t specdec_cluster_head_workspace_size(int M, int n_c, int top_k, int max_cluster);
+int specdec_cluster_head(const void* hidden, const void* cluster_emb, const void* W_sorted,
+                         const int32_t* starts, const int32_t* token_of_row, int M, int d, int V,
+                         int n_c, int top_k, int max_cluster, float temperature, uint64_t seed,
+                         int position, int mode, int32_t* out_tokens, int32_t* out_clusters,
+                         float* logits_out, void* workspace, size_t workspace_bytes,
+                         void* stream);
+
+/*
  * Reads the device status word of a workspace after synchronising `stream`:
  * SPECDEC_OK, SPECDEC_ERR_TIMEOUT or SPECDEC_ERR_TOKEN_RANGE of the last
  * call that used it. *status receives the value; the return code reports

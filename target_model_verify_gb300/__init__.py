@@ -205,6 +205,39 @@ def verify_attention(q, k_cache, v_cache, seq_lens, scale=0.0, out=None, workspa
     return out
 
 
+def cluster_head(hidden, cluster_emb, W_sorted, starts, token_of_row, top_k=1, max_cluster=None,
+                 temperature=1.0, seed=0, position=0, mode=SAMPLE, logits_out=None,
+                 workspace=None, stream=None):
+    """The drafter's clustered LM head (include/specdec_verify.h).
+
+    hidden [M, d], cluster_emb [n_c, d], W_sorted [V, d] (bf16, CUDA);
+    starts [n_c + 1] and token_of_row [V] int32 CUDA tensors. Returns
+    (tokens [M], clusters [M, top_k]) int32 on the device.
+    """
+    for t in (hidden, cluster_emb, W_sorted):
+        if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+            raise TypeError("hidden, cluster_emb and W_sorted must be contiguous bf16 CUDA tensors")
+    M, d = hidden.shape
+    n_c, V = cluster_emb.shape[0], W_sorted.shape[0]
+    if max_cluster is None:
+        max_cluster = int((starts[1:] - starts[:-1]).max())
+    dev = hidden.device
+    tokens = torch.empty(M, dtype=torch.int32, device=dev)
+    clusters = torch.empty(M, top_k, dtype=torch.int32, device=dev)
+    if workspace is None:
+        n = _b.specdec_cluster_head_workspace_size(M, n_c, top_k, max_cluster)
+        if n == 0:
+            raise SpecdecError(_b.SPECDEC_ERR_UNSUPPORTED, "cluster_head_workspace_size")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    rc = _b.specdec_cluster_head(_ptr(hidden), _ptr(cluster_emb), _ptr(W_sorted), _ptr(starts),
+                                 _ptr(token_of_row), M, d, V, n_c, top_k, max_cluster,
+                                 float(temperature), int(seed) & (2 ** 64 - 1), int(position),
+                                 int(mode), _ptr(tokens), _ptr(clusters), _ptr(logits_out),
+                                 _ptr(workspace), workspace.numel(), _stream_ptr(stream))
+    _b._check(rc, "specdec_cluster_head")
+    return tokens, clusters
+
+
 class HostStep:
     """A host-I/O verify step bound once to fixed buffers, for a decode loop.
 

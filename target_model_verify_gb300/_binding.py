@@ -59,6 +59,9 @@ _SIGNATURES = {
     "specdec_verify_attention_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "specdec_verify_attention": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp,
                                       _sz, _vp]),
+    "specdec_cluster_head_workspace_size": (_sz, [_i, _i, _i, _i]),
+    "specdec_cluster_head": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _u64, _i,
+                                  _i, _vp, _vp, _vp, _vp, _sz, _vp]),
 }
 
 _lib = None
@@ -154,6 +157,14 @@ def specdec_verify_attention_workspace_size(B, n_new, Hq, Hkv, D, Lmax) -> int:
 
 def specdec_verify_attention(*args) -> int:
     return int(lib().specdec_verify_attention(*args))
+
+
+def specdec_cluster_head_workspace_size(M, n_c, top_k, max_cluster) -> int:
+    return int(lib().specdec_cluster_head_workspace_size(M, n_c, top_k, max_cluster))
+
+
+def specdec_cluster_head(*args) -> int:
+    return int(lib().specdec_cluster_head(*args))
 
 
 def specdec_read_status(workspace_ptr: int, stream_ptr: int) -> int:

@@ -404,6 +404,39 @@ AttnPlan make_attn_plan(int B, int n_new, int Hq, int Hkv, int Lmax) {
   return p;
 }
 
+// -------------------------------------------------------- cluster head --
+
+struct ClusterPlan {
+  int max_members, sort_n;
+  size_t off_y, off_offs, off_z, off_ids, total;
+};
+
+int check_cluster_shape(int M, int d, int V, int n_c, int top_k, int max_cluster) {
+  if (M < 0 || M > 64 || d < 8 || d % 8 != 0 || d > SPECDEC_CLUSTER_MAX_D || V < 1 || n_c < 1 ||
+      top_k < 1 || top_k > SPECDEC_CLUSTER_MAX_TOP_K || top_k > n_c || max_cluster < 1 ||
+      (long long)top_k * max_cluster > SPECDEC_CLUSTER_MAX_MEMBERS)
+    return SPECDEC_ERR_UNSUPPORTED;
+  return SPECDEC_OK;
+}
+
+ClusterPlan make_cluster_plan(int M, int n_c, int top_k, int max_cluster) {
+  ClusterPlan p;
+  p.max_members = top_k * max_cluster;
+  p.sort_n = 1;
+  while (p.sort_n < p.max_members) p.sort_n <<= 1;
+  size_t off = align_up(sizeof(WsHeader));
+  p.off_y = off;
+  off = align_up(off + sizeof(float) * (size_t)M * n_c);
+  p.off_offs = off;
+  off = align_up(off + sizeof(int) * (size_t)M * (top_k + 1));
+  p.off_z = off;
+  off = align_up(off + sizeof(float) * (size_t)M * p.max_members);
+  p.off_ids = off;
+  off = align_up(off + sizeof(int) * (size_t)M * p.max_members);
+  p.total = off;
+  return p;
+}
+
 }  // namespace
 
 namespace specdec {
@@ -731,6 +764,63 @@ int specdec_verify_attention(const void* q, const void* k_cache, const void* v_c
   A.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   A.status = reinterpret_cast<int*>(ws);
   return launch_attention(A, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
+
+size_t specdec_cluster_head_workspace_size(int M, int n_c, int top_k, int max_cluster) {
+  if (check_cluster_shape(M, 8, 1, n_c, top_k, max_cluster) != SPECDEC_OK) return 0;
+  return make_cluster_plan(M, n_c, top_k, max_cluster).total;
+}
+
+int specdec_cluster_head(const void* hidden, const void* cluster_emb, const void* W_sorted,
+                         const int32_t* starts, const int32_t* token_of_row, int M, int d, int V,
+                         int n_c, int top_k, int max_cluster, float temperature, uint64_t seed,
+                         int position, int mode, int32_t* out_tokens, int32_t* out_clusters,
+                         float* logits_out, void* workspace, size_t workspace_bytes,
+                         void* stream_ptr) {
+  if (mode != SPECDEC_SAMPLE && mode != SPECDEC_GREEDY) return SPECDEC_ERR_INVALID_ARG;
+  int rc = check_cluster_shape(M, d, V, n_c, top_k, max_cluster);
+  if (rc != SPECDEC_OK) return rc;
+  if (M == 0) return SPECDEC_OK;
+  if (!hidden || !cluster_emb || !W_sorted || !starts || !token_of_row || !out_tokens ||
+      !out_clusters)
+    return SPECDEC_ERR_INVALID_ARG;
+  if ((((uintptr_t)hidden | (uintptr_t)cluster_emb | (uintptr_t)W_sorted) & 15u) != 0)
+    return SPECDEC_ERR_INVALID_ARG;
+  const bool sample = mode == SPECDEC_SAMPLE;
+  if (sample && (!(temperature > 0.f) || !std::isfinite(temperature))) return SPECDEC_ERR_INVALID_ARG;
+  const ClusterPlan pl = make_cluster_plan(M, n_c, top_k, max_cluster);
+  if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || workspace_bytes < pl.total)
+    return SPECDEC_ERR_WORKSPACE;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  ClusterLaunch L;
+  L.M = M;
+  L.d = d;
+  L.V = V;
+  L.n_c = n_c;
+  L.top_k = top_k;
+  L.max_cluster = max_cluster;
+  L.max_members = pl.max_members;
+  L.sort_n = pl.sort_n;
+  L.sample = sample ? 1 : 0;
+  L.position = position;
+  L.c = sample ? kLog2e / temperature : kLog2e;
+  L.seed = seed;
+  L.h = static_cast<const __nv_bfloat16*>(hidden);
+  L.E = static_cast<const __nv_bfloat16*>(cluster_emb);
+  L.W = static_cast<const __nv_bfloat16*>(W_sorted);
+  L.starts = starts;
+  L.token_of_row = token_of_row;
+  L.y = reinterpret_cast<float*>(ws + pl.off_y);
+  L.offs = reinterpret_cast<int*>(ws + pl.off_offs);
+  L.z = reinterpret_cast<float*>(ws + pl.off_z);
+  L.ids = reinterpret_cast<int*>(ws + pl.off_ids);
+  L.clusters = out_clusters;
+  L.tokens = out_tokens;
+  L.logits_out = logits_out;
+  L.status = reinterpret_cast<int*>(ws);
+  return launch_cluster_head(L, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
 int specdec_read_status(const void* workspace, void* stream, int32_t* status) {

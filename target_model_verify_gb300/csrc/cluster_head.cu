@@ -1,0 +1,307 @@
+// The drafter's clustered LM head ("多詞元預測視覺化指南", section 高效嵌入器):
+// score the hidden state against one embedding per token cluster, keep the
+// top-k clusters, compute token logits for their members only, and draw the
+// draft token from the softmax over those members.
+//
+// Four small kernels, each a programmatic dependent of the one before:
+//   cluster_logits   y[m, c] = h_m . E_c          one warp per cluster
+//   top_clusters     the k largest y per row      one CTA per row
+//   member_logits    z = h_m . W_r for kept rows  64 member rows per CTA
+//   draw             argmax, or the inverse CDF of softmax(z / T) in token-ID
+//                    order (members sorted by token ID in shared memory)
+// Bytes: n_c * d * 2 (cluster table) + kept rows * d * 2 per row, against
+// V * d * 2 for the full head; every kernel is latency-bound at these sizes.
+#include "kernels.h"
+
+namespace specdec {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+constexpr int kRowsPerChunk = 16;   // hidden rows staged in shared memory at once
+constexpr int kMemberBlock = 64;    // member rows per CTA of member_logits
+
+// Dot product of one bf16 row of length d (16-byte aligned, d % 8 == 0)
+// with hidden row hs (shared memory, bf16), reduced over the warp.
+__device__ __forceinline__ float warp_dot(const __nv_bfloat16* __restrict__ row,
+                                          const __nv_bfloat16* hs, int d) {
+  const int lane = threadIdx.x & 31;
+  float acc = 0.f;
+  for (int j = lane * 8; j < d; j += 256) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(row + j));
+    const uint4 b = *reinterpret_cast<const uint4*>(hs + j);
+    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
+    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float2 x = __bfloat1622float2(pa[e]);
+      const float2 y = __bfloat1622float2(pb[e]);
+      acc = fmaf(x.x, y.x, acc);
+      acc = fmaf(x.y, y.y, acc);
+    }
+  }
+  return warp_sum(acc);
+}
+
+__global__ void __launch_bounds__(kThreads) cluster_logits_kernel(const ClusterLaunch L) {
+  extern __shared__ __align__(16) uint8_t smem_h[];
+  __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(smem_h);
+  grid_dependency_wait();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int c = blockIdx.x * kWarps + warp;
+  for (int m0 = 0; m0 < L.M; m0 += kRowsPerChunk) {
+    const int nm = min(kRowsPerChunk, L.M - m0);
+    __syncthreads();
+    for (int e = threadIdx.x; e < nm * L.d / 8; e += kThreads)
+      reinterpret_cast<uint4*>(hs)[e] = __ldg(reinterpret_cast<const uint4*>(L.h + (size_t)m0 * L.d) + e);
+    __syncthreads();
+    if (c < L.n_c)
+      for (int m = 0; m < nm; ++m) {
+        const float y = warp_dot(L.E + (size_t)c * L.d, hs + (size_t)m * L.d, L.d);
+        if (lane == 0) L.y[(size_t)(m0 + m) * L.n_c + c] = y;
+      }
+  }
+}
+
+// The k largest cluster logits of row m (ties to the lower index), and the
+// member-row ranges they select.
+__global__ void __launch_bounds__(kThreads) top_clusters_kernel(const ClusterLaunch L) {
+  __shared__ float s_v[kWarps];
+  __shared__ int s_i[kWarps];
+  __shared__ int s_sel[SPECDEC_CLUSTER_MAX_TOP_K];
+  grid_dependency_wait();
+  const int m = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const float* y = L.y + (size_t)m * L.n_c;
+  for (int k = 0; k < L.top_k; ++k) {
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = threadIdx.x; c < L.n_c; c += kThreads) {
+      bool taken = false;
+      for (int j = 0; j < k; ++j) taken |= s_sel[j] == c;
+      const float v = y[c];
+      if (!taken && argmax_better(v, c, bv, bi)) {
+        bv = v;
+        bi = c;
+      }
+    }
+    warp_argmax(bv, bi);
+    if (lane == 0) {
+      s_v[warp] = bv;
+      s_i[warp] = bi;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int w = 1; w < kWarps; ++w)
+        if (argmax_better(s_v[w], s_i[w], bv, bi)) {
+          bv = s_v[w];
+          bi = s_i[w];
+        }
+      s_sel[k] = bi;
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    int off = 0;
+    bool bad = false;
+    for (int k = 0; k < L.top_k; ++k) {
+      const int c = s_sel[k];
+      const int n = L.starts[c + 1] - L.starts[c];
+      bad |= n < 0 || n > L.max_cluster;
+      L.clusters[(size_t)m * L.top_k + k] = c;
+      L.offs[(size_t)m * (L.top_k + 1) + k] = off;
+      off += max(0, min(n, L.max_cluster));
+    }
+    L.offs[(size_t)m * (L.top_k + 1) + L.top_k] = off;
+    if (bad) set_status(L.status, SPECDEC_ERR_INVALID_ARG);
+  }
+}
+
+// Logits of kept member rows: CTA (block, m) takes members
+// [64 * block, 64 * block + 64) of row m's kept list.
+__global__ void __launch_bounds__(kThreads) member_logits_kernel(const ClusterLaunch L) {
+  __shared__ __align__(16) __nv_bfloat16 hs[SPECDEC_CLUSTER_MAX_D];
+  grid_dependency_wait();
+  const int m = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int* offs = L.offs + (size_t)m * (L.top_k + 1);
+  const int total = offs[L.top_k];
+  const int i0 = blockIdx.x * kMemberBlock;
+  if (i0 >= total) return;
+  for (int e = threadIdx.x; e < L.d / 8; e += kThreads)
+    reinterpret_cast<uint4*>(hs)[e] = __ldg(reinterpret_cast<const uint4*>(L.h + (size_t)m * L.d) + e);
+  __syncthreads();
+  for (int i = i0 + warp; i < min(total, i0 + kMemberBlock); i += kWarps) {
+    int k = 0;
+    while (k + 1 < L.top_k && offs[k + 1] <= i) ++k;
+    const int c = L.clusters[(size_t)m * L.top_k + k];
+    const int r = L.starts[c] + (i - offs[k]);
+    if (r < 0 || r >= L.V) {   // starts outside the table: report, read nothing
+      if (lane == 0) set_status(L.status, SPECDEC_ERR_INVALID_ARG);
+      continue;
+    }
+    const float z = warp_dot(L.W + (size_t)r * L.d, hs, L.d);
+    if (lane == 0) {
+      const int id = L.token_of_row[r];
+      L.z[(size_t)m * L.max_members + i] = z;
+      L.ids[(size_t)m * L.max_members + i] = id;
+      if (L.logits_out != nullptr && id >= 0 && id < L.V) L.logits_out[(size_t)m * L.V + id] = z;
+    }
+  }
+}
+
+// Draft token of row m: members sorted by token ID (bitonic, shared memory),
+// then the greedy argmax or the inverse CDF of softmax(z / T).
+__global__ void __launch_bounds__(kThreads) draw_kernel(const ClusterLaunch L) {
+  extern __shared__ __align__(16) uint8_t smem_d[];
+  int* sid = reinterpret_cast<int*>(smem_d);
+  float* sz = reinterpret_cast<float*>(sid + L.sort_n);
+  __shared__ float s_red[kWarps];
+  __shared__ int s_redi[kWarps];
+  __shared__ int s_tok, s_last;
+  grid_dependency_wait();
+  const int m = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int total = L.offs[(size_t)m * (L.top_k + 1) + L.top_k];
+  const int n = L.sort_n;   // power of two >= max_members
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    const bool in = i < total;
+    sid[i] = in ? L.ids[(size_t)m * L.max_members + i] : 0x7fffffff;
+    sz[i] = in ? L.z[(size_t)m * L.max_members + i] : -INFINITY;
+  }
+  __syncthreads();
+  // bitonic sort by token ID (ascending)
+  for (int size = 2; size <= n; size <<= 1)
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < n; i += kThreads) {
+        const int j = i ^ stride;
+        if (j > i) {
+          const bool up = (i & size) == 0;
+          if ((sid[i] > sid[j]) == up) {
+            const int ti = sid[i];
+            sid[i] = sid[j];
+            sid[j] = ti;
+            const float tz = sz[i];
+            sz[i] = sz[j];
+            sz[j] = tz;
+          }
+        }
+      }
+      __syncthreads();
+    }
+  // max logit (and its lowest token ID: members are in token-ID order)
+  float bv = -INFINITY;
+  int bi = 0x7fffffff;
+  for (int i = threadIdx.x; i < total; i += kThreads)
+    if (argmax_better(sz[i], sid[i], bv, bi)) {
+      bv = sz[i];
+      bi = sid[i];
+    }
+  warp_argmax(bv, bi);
+  if (lane == 0) {
+    s_red[warp] = bv;
+    s_redi[warp] = bi;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kWarps; ++w)
+      if (argmax_better(s_red[w], s_redi[w], bv, bi)) {
+        bv = s_red[w];
+        bi = s_redi[w];
+      }
+    s_red[0] = bv;
+    s_redi[0] = bi;
+  }
+  __syncthreads();
+  const float zmax = s_red[0];
+  if (!L.sample) {
+    if (threadIdx.x == 0) L.tokens[m] = total > 0 ? s_redi[0] : -1;
+    return;
+  }
+  // Weights exp2((z - zmax) c) in token-ID order; the draw inverts their
+  // prefix sum at u * S: contiguous segments per thread, a block scan of the
+  // segment sums, then the first weighted token whose running sum passes t.
+  for (int i = threadIdx.x; i < total; i += kThreads) sz[i] = exp2f((sz[i] - zmax) * L.c);
+  __syncthreads();
+  const int per = (total + kThreads - 1) / kThreads;
+  const int a = min(total, threadIdx.x * per), e = min(total, a + per);
+  float ts = 0.f;
+  for (int i = a; i < e; ++i) ts += sz[i];
+  float incl = ts;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) s_red[warp] = incl;
+  if (threadIdx.x == 0) {
+    s_tok = 0x7fffffff;
+    s_last = -1;
+  }
+  __syncthreads();
+  float before = 0.f, S = 0.f;
+  for (int w = 0; w < kWarps; ++w) {
+    if (w < warp) before += s_red[w];
+    S += s_red[w];
+  }
+  const float t = draft_uniform(L.seed, m, L.position) * S;
+  float run = before + (incl - ts);
+  int cand = 0x7fffffff, lastp = -1;
+  for (int i = a; i < e; ++i) {
+    run += sz[i];
+    if (sz[i] > 0.f) lastp = sid[i];
+    if (cand == 0x7fffffff && sz[i] > 0.f && run > t) cand = sid[i];
+  }
+  if (cand != 0x7fffffff) atomicMin(&s_tok, cand);
+  if (lastp >= 0) atomicMax(&s_last, lastp);
+  __syncthreads();
+  if (threadIdx.x == 0) L.tokens[m] = s_tok != 0x7fffffff ? s_tok : s_last;   // t rounded past S
+}
+
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, size_t smem, const ClusterLaunch& L,
+                       cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {const_cast<ClusterLaunch*>(&L)};
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+}  // namespace
+
+cudaError_t launch_cluster_head(const ClusterLaunch& L, cudaStream_t stream) {
+  const size_t smem1 = (size_t)kRowsPerChunk * L.d * 2;
+  const size_t smem4 = (size_t)L.sort_n * 8;
+  static int set[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64 || !set[dev]) {
+    e = cudaFuncSetAttribute(cluster_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kRowsPerChunk * SPECDEC_CLUSTER_MAX_D * 2);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(draw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             SPECDEC_CLUSTER_MAX_MEMBERS * 8);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < 64) set[dev] = 1;
+  }
+  e = launch_pdl((const void*)cluster_logits_kernel, dim3((L.n_c + kWarps - 1) / kWarps),
+                 dim3(kThreads), smem1, L, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl((const void*)top_clusters_kernel, dim3(L.M), dim3(kThreads), 0, L, stream);
+  if (e != cudaSuccess) return e;
+  e = launch_pdl((const void*)member_logits_kernel,
+                 dim3((L.max_members + kMemberBlock - 1) / kMemberBlock, L.M), dim3(kThreads), 0, L,
+                 stream);
+  if (e != cudaSuccess) return e;
+  return launch_pdl((const void*)draw_kernel, dim3(L.M), dim3(kThreads), smem4, L, stream);
+}
+
+}  // namespace specdec

@@ -95,6 +95,10 @@ __device__ __forceinline__ float accept_uniform(uint64_t seed, int b, int i) {
 __device__ __forceinline__ float sample_uniform(uint64_t seed, int b, int i) {
   return (float)uniform24(seed, b, i, 1) * 5.9604644775390625e-08f;
 }
+// The draft draw's uniform (purpose 2), same map as the sampling uniform.
+__device__ __forceinline__ float draft_uniform(uint64_t seed, int b, int i) {
+  return (float)uniform24(seed, b, i, 2) * 5.9604644775390625e-08f;
+}
 
 // ------------------------------------------------------ warp reductions --
 

@@ -112,6 +112,27 @@ struct AttnLaunch {
 cudaError_t launch_attention(const AttnLaunch& A, cudaStream_t stream);
 int attn_smem_bytes();
 
+// The drafter's clustered LM head.
+struct ClusterLaunch {
+  int M, d, V, n_c, top_k, max_cluster, max_members, sort_n, sample, position;
+  float c;                           // log2(e) / T
+  uint64_t seed;
+  const __nv_bfloat16* h;            // [M, d]
+  const __nv_bfloat16* E;            // [n_c, d]
+  const __nv_bfloat16* W;            // [V, d] rows grouped by cluster
+  const int32_t* starts;             // [n_c + 1]
+  const int32_t* token_of_row;       // [V]
+  float* y;                          // [M, n_c] cluster logits
+  int* offs;                         // [M, top_k + 1] kept members' prefix
+  float* z;                          // [M, max_members] kept members' logits
+  int* ids;                          // [M, max_members] their token IDs
+  int32_t* clusters;                 // [M, top_k]
+  int32_t* tokens;                   // [M]
+  float* logits_out;                 // [M, V] or null
+  int* status;
+};
+cudaError_t launch_cluster_head(const ClusterLaunch& L, cudaStream_t stream);
+
 cudaError_t launch_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose, float* out,
                                    cudaStream_t stream);
 

@@ -618,10 +618,9 @@ def run_cluster_head(args):
     tor = torch.randperm(V, generator=g, device=device).int()
     h = torch.randn(M, d, generator=g, device=device)
     h = (h / h.pow(2).mean(-1, keepdim=True).sqrt() * 3.0).to(torch.bfloat16)
-    ws = torch.empty(tv._b.specdec_cluster_head_workspace_size(M, n_c, K, size), dtype=torch.uint8,
-                     device=device)
-    step = lambda i: tv.cluster_head(h, E, W, starts, tor, top_k=K, max_cluster=size, seed=i,
-                                     position=i, workspace=ws)
+    head = tv.ClusterHeadStep(h, E, W, starts, tor, top_k=K, max_cluster=size)
+    ws = head.workspace
+    step = lambda i: head(seed=i, position=i)
     Kst, Wm = args.steps, args.warmup
     for i in range(Wm):
         step(i)

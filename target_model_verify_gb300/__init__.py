@@ -238,6 +238,52 @@ def cluster_head(hidden, cluster_emb, W_sorted, starts, token_of_row, top_k=1, m
     return tokens, clusters
 
 
+class ClusterHeadStep:
+    """The clustered LM head bound once to fixed device buffers, for a draft loop.
+
+    Same contract as cluster_head(); the drafter refills `hidden` in place
+    between calls and each call passes only the seed and the position.
+    The results land in self.tokens [M] and self.clusters [M, top_k].
+    """
+
+    def __init__(self, hidden, cluster_emb, W_sorted, starts, token_of_row, top_k=1,
+                 max_cluster=None, temperature=1.0, mode=SAMPLE, logits_out=None, workspace=None,
+                 stream=None):
+        for t in (hidden, cluster_emb, W_sorted):
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise TypeError("hidden, cluster_emb and W_sorted must be contiguous bf16 CUDA tensors")
+        M, d = hidden.shape
+        n_c, V = cluster_emb.shape[0], W_sorted.shape[0]
+        if max_cluster is None:
+            max_cluster = int((starts[1:] - starts[:-1]).max())
+        dev = hidden.device
+        self.tokens = torch.empty(M, dtype=torch.int32, device=dev)
+        self.clusters = torch.empty(M, top_k, dtype=torch.int32, device=dev)
+        if workspace is None:
+            n = _b.specdec_cluster_head_workspace_size(M, n_c, top_k, max_cluster)
+            if n == 0:
+                raise SpecdecError(_b.SPECDEC_ERR_UNSUPPORTED, "cluster_head_workspace_size")
+            workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.workspace = workspace
+        self._keep = (hidden, cluster_emb, W_sorted, starts, token_of_row, logits_out)
+        self._fn = _b.lib().specdec_cluster_head
+        a = _b._SIGNATURES["specdec_cluster_head"][1]
+        vals = [_ptr(hidden), _ptr(cluster_emb), _ptr(W_sorted), _ptr(starts), _ptr(token_of_row),
+                M, d, V, n_c, top_k, max_cluster, float(temperature), 0, 0, int(mode),
+                _ptr(self.tokens), _ptr(self.clusters), _ptr(logits_out), _ptr(workspace),
+                workspace.numel(), _stream_ptr(stream)]
+        self._args = [t(v) for t, v in zip(a, vals)]
+        self._seed, self._position = self._args[12], self._args[13]
+
+    def __call__(self, seed, position=0):
+        self._seed.value = int(seed) & (2 ** 64 - 1)
+        self._position.value = int(position)
+        rc = self._fn(*self._args)
+        if rc != 0:
+            _b._check(rc, "specdec_cluster_head")
+        return self.tokens, self.clusters
+
+
 class HostStep:
     """A host-I/O verify step bound once to fixed buffers, for a decode loop.
 
@@ -296,4 +342,6 @@ def philox_uniforms(seed, B, n_pos, purpose, device="cuda", stream=None):
 
 
 __all__ = ["verify", "verify_host", "alloc_workspace", "workspace_bytes", "read_status",
-           "philox_uniforms", "status_string", "SpecdecError", "SAMPLE", "GREEDY"]
+           "philox_uniforms", "status_string", "SpecdecError", "SAMPLE", "GREEDY", "HostStep",
+           "verify_tree", "tree_workspace_bytes", "alloc_tree_workspace", "verify_attention",
+           "attention_workspace_bytes", "cluster_head", "ClusterHeadStep"]

@@ -793,7 +793,6 @@ int specdec_cluster_head(const void* hidden, const void* cluster_emb, const void
     return SPECDEC_ERR_WORKSPACE;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
   char* ws = static_cast<char*>(workspace);
-  if (cudaMemsetAsync(ws, 0, sizeof(int), stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
   ClusterLaunch L;
   L.M = M;
   L.d = d;

@@ -6,7 +6,7 @@
 // Four small kernels, each a programmatic dependent of the one before:
 //   cluster_logits   y[m, c] = h_m . E_c          one warp per cluster
 //   top_clusters     the k largest y per row      one CTA per row
-//   member_logits    z = h_m . W_r for kept rows  64 member rows per CTA
+//   member_logits    z = h_m . W_r for kept rows  one kept row per warp
 //   draw             argmax, or the inverse CDF of softmax(z / T) in token-ID
 //                    order (members sorted by token ID in shared memory)
 // Bytes: n_c * d * 2 (cluster table) + kept rows * d * 2 per row, against
@@ -19,25 +19,38 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerChunk = 16;   // hidden rows staged in shared memory at once
-constexpr int kMemberBlock = 64;    // member rows per CTA of member_logits
+constexpr int kMemberBlock = kWarps;   // member rows per CTA of member_logits: one per warp
+constexpr int kDotDepth = 4;            // 16-byte loads a lane keeps in flight in warp_dot
 
 // Dot product of one bf16 row of length d (16-byte aligned, d % 8 == 0)
-// with hidden row hs (shared memory, bf16), reduced over the warp.
+// with hidden row hs (shared memory, bf16), reduced over the warp. Each lane
+// issues kDotDepth loads before it consumes any, so one warp keeps
+// 32 * kDotDepth * 16 bytes of the row in flight.
 __device__ __forceinline__ float warp_dot(const __nv_bfloat16* __restrict__ row,
                                           const __nv_bfloat16* hs, int d) {
   const int lane = threadIdx.x & 31;
   float acc = 0.f;
-  for (int j = lane * 8; j < d; j += 256) {
-    const uint4 a = __ldg(reinterpret_cast<const uint4*>(row + j));
-    const uint4 b = *reinterpret_cast<const uint4*>(hs + j);
-    const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a);
-    const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+  for (int j0 = lane * 8; j0 < d; j0 += 256 * kDotDepth) {
+    uint4 a[kDotDepth];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 x = __bfloat1622float2(pa[e]);
-      const float2 y = __bfloat1622float2(pb[e]);
-      acc = fmaf(x.x, y.x, acc);
-      acc = fmaf(x.y, y.y, acc);
+    for (int u = 0; u < kDotDepth; ++u) {
+      const int j = j0 + u * 256;
+      a[u] = j < d ? __ldg(reinterpret_cast<const uint4*>(row + j)) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int u = 0; u < kDotDepth; ++u) {
+      const int j = j0 + u * 256;
+      if (j >= d) break;
+      const uint4 b = *reinterpret_cast<const uint4*>(hs + j);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&a[u]);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 x = __bfloat1622float2(pa[e]);
+        const float2 y = __bfloat1622float2(pb[e]);
+        acc = fmaf(x.x, y.x, acc);
+        acc = fmaf(x.y, y.y, acc);
+      }
     }
   }
   return warp_sum(acc);
@@ -46,7 +59,11 @@ __device__ __forceinline__ float warp_dot(const __nv_bfloat16* __restrict__ row,
 __global__ void __launch_bounds__(kThreads) cluster_logits_kernel(const ClusterLaunch L) {
   extern __shared__ __align__(16) uint8_t smem_h[];
   __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(smem_h);
+  grid_launch_dependents();
   grid_dependency_wait();
+  // The status word is cleared here, after the previous work on the stream
+  // has finished; the later kernels of the chain only set it.
+  if (blockIdx.x == 0 && threadIdx.x == 0) *L.status = SPECDEC_OK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
   for (int m0 = 0; m0 < L.M; m0 += kRowsPerChunk) {
@@ -69,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) top_clusters_kernel(const ClusterLau
   __shared__ float s_v[kWarps];
   __shared__ int s_i[kWarps];
   __shared__ int s_sel[SPECDEC_CLUSTER_MAX_TOP_K];
+  grid_launch_dependents();
   grid_dependency_wait();
   const int m = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -118,9 +136,10 @@ __global__ void __launch_bounds__(kThreads) top_clusters_kernel(const ClusterLau
 }
 
 // Logits of kept member rows: CTA (block, m) takes members
-// [64 * block, 64 * block + 64) of row m's kept list.
+// [8 * block, 8 * block + 8) of row m's kept list, one per warp.
 __global__ void __launch_bounds__(kThreads) member_logits_kernel(const ClusterLaunch L) {
   __shared__ __align__(16) __nv_bfloat16 hs[SPECDEC_CLUSTER_MAX_D];
+  grid_launch_dependents();
   grid_dependency_wait();
   const int m = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

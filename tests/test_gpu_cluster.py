@@ -99,3 +99,25 @@ def test_cluster_head_bad_starts_set_status():
     tv.cluster_head(x["h"], x["E"], x["W"], starts, x["tor"], top_k=8, max_cluster=512,
                     mode=ov.GREEDY, workspace=ws)
     assert tv.read_status(ws) == tv._b.SPECDEC_ERR_INVALID_ARG
+    # the next good call on the same workspace clears the status word
+    tv.cluster_head(x["h"], x["E"], x["W"], x["starts"], x["tor"], top_k=8, max_cluster=512,
+                    mode=ov.GREEDY, workspace=ws)
+    assert tv.read_status(ws) == 0
+
+
+def test_prepared_cluster_head_rereads_hidden():
+    """ClusterHeadStep gives cluster_head()'s tokens, and sees hidden refilled in place."""
+    import target_model_verify_gb300 as tv
+    x = _head(11, 16, 256, 4000, 32)
+    step = tv.ClusterHeadStep(x["h"], x["E"], x["W"], x["starts"], x["tor"], top_k=2,
+                              temperature=0.9)
+    for seed, pos in ((1, 0), (1, 3), (2, 3)):
+        tok, cl = tv.cluster_head(x["h"], x["E"], x["W"], x["starts"], x["tor"], top_k=2,
+                                  temperature=0.9, seed=seed, position=pos)
+        got_tok, got_cl = step(seed, pos)
+        assert torch.equal(tok, got_tok) and torch.equal(cl, got_cl)
+    x["h"].copy_(x["h"].flip(0))
+    want = _compare(x, 2, 0.9, 2, ov.SAMPLE, position=3)
+    got, _ = step(2, 3)
+    torch.cuda.synchronize()
+    assert np.array_equal(got.cpu().numpy(), want)

@@ -205,6 +205,11 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
@@ -382,6 +387,14 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t smem, in
   asm volatile(
       "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(tmap),
       "r"(smem), "r"(x), "r"(y)
+      : "memory");
+}
+// The same with an L2 eviction-priority policy for the written lines.
+__device__ __forceinline__ void tma_store_2d_hint(const void* tmap, uint32_t smem, int x, int y,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3}], [%1], %4;"
+      ::"l"(tmap), "r"(smem), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
 // Bulk prefetch of [addr, addr + bytes) into L2 (16-byte aligned, bytes a

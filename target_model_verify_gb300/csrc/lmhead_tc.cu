@@ -295,7 +295,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ---------------------------------------------------- TMA producer --
-      const uint64_t pol_w = policy_evict_first();
+      // A W tile read by one token tile leaves L2 first; with several token
+      // tiles, the other tiles' CTAs read the same W tile at about the same
+      // time, so it keeps the normal priority and outlives the logit stores.
+      const uint64_t pol_w = p.n_tt > 1 ? policy_evict_normal() : policy_evict_first();
       const uint64_t pol_h = policy_evict_last();
       int s = 0;
       uint32_t ph = 0;
@@ -594,7 +597,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {
-                tma_store_2d(&tmap_z, zstg, v0, mw);
+                tma_store_2d_hint(&tmap_z, zstg, v0, mw, policy_evict_first());
                 bulk_commit();
               }
             }

@@ -141,6 +141,21 @@ bool encode_bf16_rows3d(CUtensorMap* map, const void* base, int rows, int cols, 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// One layer's K or V cache [B, Lmax, Hkv, 128] (bf16) as a 4-D tensor
+// {128, Hkv, Lmax, B} with a {64, 1, 64, 1} box (64 keys x 64 dims) and the
+// 128-byte swizzle; keys past Lmax read 0.
+bool encode_kv_cache(CUtensorMap* map, const void* base, int B, int Lmax, int Hkv) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {128, (cuuint64_t)Hkv, (cuuint64_t)Lmax, (cuuint64_t)B};
+  const cuuint64_t strides[3] = {256, (cuuint64_t)Hkv * 256, (cuuint64_t)Lmax * Hkv * 256};
+  const cuuint32_t box[4] = {64, 1, 64, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct Extras {
   float* logits_out = nullptr;
   float* lse_p = nullptr;
@@ -375,17 +390,27 @@ int check_attn_shape(int B, int n_new, int Hq, int Hkv, int D, int Lmax) {
   return SPECDEC_OK;
 }
 
-// Splits of the key range: none once the (sequence, KV head) pairs alone
-// fill two waves of a 152-SM part; otherwise enough for four waves, at least
-// 256 keys each (fixed targets, so the workspace size does not depend on
-// the device).
+// Splits of the key range. The split kernel keeps two CTAs resident per SM
+// (one when the query rows need four row tiles), so a 152-SM part holds
+// `slots` CTAs at once. Once the (sequence, KV head) pairs alone fill that,
+// no split. Otherwise the splits stay within one wave (a small last wave
+// would run with too few CTAs to keep HBM busy) and aim at 1.5 CTAs per SM,
+// at least 256 keys each (fixed targets, so the workspace size does not
+// depend on the device).
 AttnPlan make_attn_plan(int B, int n_new, int Hq, int Hkv, int Lmax) {
   AttnPlan p;
   const long long pairs = (long long)B * Hkv;
-  long long want = pairs >= 304 ? 1 : pairs > 0 ? (608 + pairs - 1) / pairs : 1;
-  const long long most = (Lmax + 255) / 256;
-  if (want > most) want = most;
-  if (want < 1) want = 1;
+  const int n_mt = (n_new * (Hq / Hkv) + 15) / 16;
+  const long long slots = 152ll * (n_mt <= 3 ? 2 : 1);
+  const long long target = 228;
+  long long want = 1;
+  if (pairs > 0 && pairs < slots) {
+    want = (target + pairs - 1) / pairs;
+    if (want > slots / pairs) want = slots / pairs;
+    const long long most = (Lmax + 255) / 256;
+    if (want > most) want = most;
+    if (want < 1) want = 1;
+  }
   int split = (int)((Lmax + want - 1) / want);
   split = (split + 63) / 64 * 64;
   p.split_len = split;
@@ -753,6 +778,7 @@ int specdec_verify_attention(const void* q, const void* k_cache, const void* v_c
   A.Lmax = Lmax;
   A.n_splits = pl.n_splits;
   A.split_len = pl.split_len;
+  A.n_stages = attn_n_stages(B, n_new, Hq, Hkv);
   A.scale_log2 = (scale > 0.f ? scale : 1.f / std::sqrt((float)D)) * kLog2e;
   A.q = static_cast<const __nv_bfloat16*>(q);
   A.k = static_cast<const __nv_bfloat16*>(k_cache);
@@ -763,7 +789,10 @@ int specdec_verify_attention(const void* q, const void* k_cache, const void* v_c
   A.part_l = reinterpret_cast<float*>(ws + pl.off_l);
   A.part_o = reinterpret_cast<float*>(ws + pl.off_o);
   A.status = reinterpret_cast<int*>(ws);
-  return launch_attention(A, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+  CUtensorMap tk, tv;
+  if (!encode_kv_cache(&tk, k_cache, B, Lmax, Hkv) || !encode_kv_cache(&tv, v_cache, B, Lmax, Hkv))
+    return SPECDEC_ERR_CUDA;
+  return launch_attention(A, tk, tv, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 
 size_t specdec_cluster_head_workspace_size(int M, int n_c, int top_k, int max_cluster) {

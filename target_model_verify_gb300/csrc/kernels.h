@@ -98,6 +98,7 @@ cudaError_t launch_tree_walk(const TreeLaunch& L, cudaStream_t stream);
 // Verify-step attention (one layer): split-KV partials and their merge.
 struct AttnLaunch {
   int B, n_new, Hq, Hkv, Lmax, n_splits, split_len;
+  int n_stages;                      // K/V blocks in flight per CTA (attn_n_stages)
   float scale_log2;                  // softmax scale times log2(e)
   const __nv_bfloat16* q;            // [B, n_new, Hq, 128]
   const __nv_bfloat16* k;            // [B, Lmax, Hkv, 128]
@@ -109,8 +110,12 @@ struct AttnLaunch {
   float* part_o;                     // [B, Hkv, n_splits, 64, 128]
   int* status;
 };
-cudaError_t launch_attention(const AttnLaunch& A, cudaStream_t stream);
-int attn_smem_bytes();
+// tmap_k, tmap_v: the caches as 4-D bf16 tensors {128, Hkv, Lmax, B} with a
+// {64, 1, 64, 1} box and the 128-byte swizzle.
+cudaError_t launch_attention(const AttnLaunch& A, const CUtensorMap& tmap_k,
+                             const CUtensorMap& tmap_v, cudaStream_t stream);
+int attn_n_stages(int B, int n_new, int Hq, int Hkv);
+int attn_smem_bytes(int n_mt, int n_stages);
 
 // The drafter's clustered LM head.
 struct ClusterLaunch {

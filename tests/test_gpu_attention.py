@@ -47,6 +47,8 @@ def _check(q, k, v, lens, out, rows=None):
     (2, 5, 4, 4, 1000),      # no grouping, ragged last block
     (5, 8, 16, 2, 777),      # 64 query rows per KV head (the limit)
     (64, 5, 32, 8, 256),     # enough KV heads for one split per sequence
+    (1, 5, 4, 1, 16400),     # one KV head: 64 splits, merged 32 per lane pass
+    (2, 8, 64, 8, 700),      # 64 query rows per KV head: four row tiles, two stages
 ])
 def test_attention_matches_oracle(B, n_new, Hq, Hkv, Lmax):
     import target_model_verify_gb300 as tv

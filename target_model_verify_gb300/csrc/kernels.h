@@ -74,8 +74,11 @@ struct SampleLaunch {
 cudaError_t launch_sample(const SampleLaunch& L, cudaStream_t stream);
 
 // Tree verification walk: one cluster of kTreeCluster CTAs per sequence
-// (sampling; the CTAs split the vocabulary) or one CTA (greedy).
+// (sampling; the CTAs split the vocabulary), kTreeClusterWide when every
+// sequence's cluster of that size can be resident at once, or one CTA
+// (greedy).
 constexpr int kTreeCluster = 8;
+constexpr int kTreeClusterWide = 16;
 struct TreeLaunch {
   int B, N, V, P, Pq, mode, vec;
   float c;

@@ -13,8 +13,9 @@
 //   becomes the node; otherwise draw one token from the last residual (or
 //   from p_u) by inverting its prefix sum in token-ID order at t = u * S.
 //
-// Sampling: one cluster of kTreeCluster CTAs per sequence, each CTA owning a
-// contiguous slice of the vocabulary. Every decision is computed identically
+// Sampling: one cluster of kTreeCluster CTAs per sequence (kTreeClusterWide
+// while every sequence's cluster of that size can run at once), each CTA
+// owning a contiguous slice of the vocabulary. Every decision is computed identically
 // by all CTAs of the cluster (same records, same values, sums exchanged
 // through distributed shared memory and added in rank order), so their
 // control flow never diverges and every cluster barrier is reached by all.
@@ -44,10 +45,10 @@ struct Shared {
   float Sinv[SPECDEC_MAX_TREE_NODES + 1];   // and their reciprocals
   NodeStats node[SPECDEC_MAX_TREE_NODES];   // every node's normalisers and argmax
   float cz[SPECDEC_MAX_TREE_NODES], cd[SPECDEC_MAX_TREE_NODES];   // child's logits at its parent
-  float xv[2];              // cluster exchange slots (double buffered)
-  int xi[2];
-  float allv[kTreeCluster];
-  int alli[kTreeCluster];
+  float xv[2][kTreeClusterWide];   // cluster exchange slots, written by every CTA
+  int xi[2][kTreeClusterWide];     // of the cluster (double buffered)
+  float allv[kTreeClusterWide];
+  int alli[kTreeClusterWide];
   float wm[kWarps], ws[kWarps], wav[kWarps];
   int wai[kWarps];
   int16_t first_child[SPECDEC_MAX_TREE_NODES], next_sibling[SPECDEC_MAX_TREE_NODES];
@@ -56,41 +57,72 @@ struct Shared {
   int last_found;
 };
 
-// Every node's records folded, one warp per node (records lane-strided,
-// then a butterfly): the node's target (max, sum) and argmax, and in
+constexpr int kFoldDepth = 8;   // record loads a lane keeps in flight while folding
+
+// 2^x by the PTX approximate base-2 exponential (flushes subnormals; -inf
+// gives 0): one instruction per weight in the vocabulary passes.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Every node's records folded, one half-warp per node (records
+// lane-strided with kFoldDepth loads in flight per lane, then a butterfly
+// over the 16 lanes): the node's target (max, sum) and argmax, and in
 // sampling mode its draft (max, sum). All in a fixed order, so every CTA of
 // a cluster gets the same values.
 __device__ void fold_all_nodes(const TreeLaunch& L, int b, bool sample, Shared& sh) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int n = warp; n < L.N; n += kWarps) {
-    const size_t m = (size_t)b * L.N + n;
+  const int hl = lane & 15;
+  for (int n0 = 2 * warp; n0 < L.N; n0 += 2 * kWarps) {
+    const int n = n0 + (lane >> 4);
+    const bool valid = n < L.N;              // both halves run every shuffle below
+    const size_t m = (size_t)b * L.N + (valid ? n : n0);
     float pm = -INFINITY, ps = 0.f, av = -INFINITY;
     int ai = 0x7fffffff;
+    float qm = -INFINITY, qs = 0.f;
     const PartialP* row = L.pp + m * L.P;
-    for (int t = lane; t < L.P; t += 32) {
-      const PartialP x = row[t];
-      if (sample) softmax_merge(pm, ps, x.m, x.s, L.c);
-      if (argmax_better(x.amax_v, x.amax_i, av, ai)) {
-        av = x.amax_v;
-        ai = x.amax_i;
+    const PartialQ* qrow = L.pq + m * L.Pq;
+    const int np = valid ? L.P : 0, nq = (valid && sample) ? L.Pq : 0;
+    for (int t0 = hl; t0 < np || t0 < nq; t0 += 16 * kFoldDepth) {
+      PartialP x[kFoldDepth];
+      PartialQ y[kFoldDepth];
+#pragma unroll
+      for (int j = 0; j < kFoldDepth; ++j) {
+        const int t = t0 + 16 * j;
+        if (t < np) x[j] = row[t];
+        if (t < nq) y[j] = qrow[t];
+      }
+#pragma unroll
+      for (int j = 0; j < kFoldDepth; ++j) {
+        const int t = t0 + 16 * j;
+        if (t < np) {
+          if (sample) softmax_merge(pm, ps, x[j].m, x[j].s, L.c);
+          if (argmax_better(x[j].amax_v, x[j].amax_i, av, ai)) {
+            av = x[j].amax_v;
+            ai = x[j].amax_i;
+          }
+        }
+        if (t < nq) softmax_merge(qm, qs, y[j].m, y[j].s, L.c);
       }
     }
-    float qm = -INFINITY, qs = 0.f;
-    if (sample) {
-      const PartialQ* qrow = L.pq + m * L.Pq;
-      for (int t = lane; t < L.Pq; t += 32) softmax_merge(qm, qs, qrow[t].m, qrow[t].s, L.c);
-    }
 #pragma unroll
-    for (int o = 16; o; o >>= 1) {
+    for (int o = 8; o; o >>= 1) {
       const float m2 = __shfl_xor_sync(0xffffffffu, pm, o);
       const float s2 = __shfl_xor_sync(0xffffffffu, ps, o);
       softmax_merge(pm, ps, m2, s2, L.c);
       const float qm2 = __shfl_xor_sync(0xffffffffu, qm, o);
       const float qs2 = __shfl_xor_sync(0xffffffffu, qs, o);
       softmax_merge(qm, qs, qm2, qs2, L.c);
+      const float av2 = __shfl_xor_sync(0xffffffffu, av, o);
+      const int ai2 = __shfl_xor_sync(0xffffffffu, ai, o);
+      if (argmax_better(av2, ai2, av, ai)) {
+        av = av2;
+        ai = ai2;
+      }
     }
-    warp_argmax(av, ai);
-    if (lane == 0) {
+    if (valid && hl == 0) {
       NodeStats st;
       st.mp = pm;
       st.lsp = log2f(ps);
@@ -108,9 +140,9 @@ __device__ void fold_all_nodes(const TreeLaunch& L, int b, bool sample, Shared& 
 // (multiplied by the reciprocal, the same way in every pass and test).
 __device__ __forceinline__ float weight(float z, float d, const NodeStats& st, float c, int lev,
                                         const float* Sinv) {
-  const float p = exp2f((z - st.mp) * c - st.lsp);
+  const float p = ex2((z - st.mp) * c - st.lsp);
   if (lev == 0) return p;
-  const float q = exp2f((d - st.mq) * c - st.lsq);
+  const float q = ex2((d - st.mq) * c - st.lsq);
   float f = p;
   for (int j = 1; j < lev; ++j) f = fmaxf(0.f, f - q) * Sinv[j];
   return fmaxf(0.f, f - q);
@@ -161,8 +193,8 @@ __device__ __forceinline__ void weights4(const TreeLaunch& L, size_t m, int v, i
   weights_of(load4(L, m, v, hi, lev), st, L.c, lev, S, w);
 }
 
-// Chunk sums of this CTA's slice [lo, hi) at level `lev`; returns the
-// slice total (chunk sums added in chunk order). Each warp takes chunks
+// Chunk sums of this CTA's slice [lo, hi) at level `lev` (kept in
+// sh.chunk for a draw); returns the slice total and sets sh.last_found. Each warp takes chunks
 // warp, warp + 8, ...; with vector loads the loads of kBatch chunks are
 // issued (predicated, straight-line) before any arithmetic, so they are in
 // flight together.
@@ -210,29 +242,22 @@ __device__ float slice_pass(const TreeLaunch& L, size_t m, int lo, int hi, int l
   }
   __syncthreads();
   if (warp == 0) {
-    // Inclusive prefix in chunk order, 32 chunks at a time with a carry.
-    float carry = 0.f;
-    for (int g = 0; g < nch; g += 32) {
-      const int k = g + lane;
-      const float x = k < nch ? sh.chunk[k] : 0.f;
-      float incl = x;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
-      }
-      if (k < nch) sh.pre[k] = carry + incl;
-      carry += __shfl_sync(0xffffffffu, incl, 31);
-    }
-    // The last chunk holding weight (for a draw point rounded up to the total).
+    // The slice total (fixed order: lane-strided, then a butterfly) and the
+    // last chunk holding weight (for a draw point rounded up to the total).
+    float tot = 0.f;
     int lastc = -1;
-    for (int g = ((nch - 1) / 32) * 32; g >= 0 && lastc < 0; g -= 32) {
-      const int k = g + lane;
-      const unsigned pos = __ballot_sync(0xffffffffu, k < nch && sh.chunk[k] > 0.f);
-      if (pos) lastc = g + 31 - __clz(pos);
+    for (int k = lane; k < nch; k += 32) {
+      const float x = sh.chunk[k];
+      tot += x;
+      if (x > 0.f) lastc = k;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      tot += __shfl_xor_sync(0xffffffffu, tot, o);
+      lastc = max(lastc, __shfl_xor_sync(0xffffffffu, lastc, o));
     }
     if (lane == 0) {
-      sh.flag = __float_as_int(carry);
+      sh.flag = __float_as_int(tot);
       sh.last_found = lastc;
     }
   }
@@ -240,18 +265,46 @@ __device__ float slice_pass(const TreeLaunch& L, size_t m, int lo, int hi, int l
   return __int_as_float(sh.flag);
 }
 
+// Inclusive prefix of the slice's chunk sums in chunk order (warp 0 only),
+// 32 chunks at a time with a carry, into sh.pre.
+__device__ void chunk_prefix(int nch, Shared& sh) {
+  const int lane = threadIdx.x & 31;
+  float carry = 0.f;
+  for (int g = 0; g < nch; g += 32) {
+    const int k = g + lane;
+    const float x = k < nch ? sh.chunk[k] : 0.f;
+    float incl = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (k < nch) sh.pre[k] = carry + incl;
+    carry += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  __syncwarp();
+}
+
 // Every CTA of the cluster publishes (v, i); all get every CTA's pair in
-// rank order.
+// rank order. Each CTA stores its pair into every CTA's slot for it, so
+// after the cluster barrier (release / acquire) all reads are local.
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 template <int kCW>
 __device__ void exchange(float v, int i, int& par, Shared& sh) {
-  if (threadIdx.x == 0) {
-    sh.xv[par] = v;
-    sh.xi[par] = i;
+  const int rank = (int)cluster_ctarank();
+  if (threadIdx.x < kCW) {
+    st_cluster_f32(mapa_shared(smem_u32(&sh.xv[par][rank]), threadIdx.x), v);
+    st_cluster_s32(mapa_shared(smem_u32(&sh.xi[par][rank]), threadIdx.x), i);
   }
   cluster_sync_all();
   if (threadIdx.x < kCW) {
-    sh.allv[threadIdx.x] = ld_cluster_f32(mapa_shared(smem_u32(&sh.xv[par]), threadIdx.x));
-    sh.alli[threadIdx.x] = ld_cluster_s32(mapa_shared(smem_u32(&sh.xi[par]), threadIdx.x));
+    sh.allv[threadIdx.x] = sh.xv[par][threadIdx.x];
+    sh.alli[threadIdx.x] = sh.xi[par][threadIdx.x];
   }
   __syncthreads();
   par ^= 1;
@@ -300,14 +353,21 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeLaunch
   // Every node's statistics, and every child's target and draft logit at
   // its parent's row, before the walk: the walk itself then waits only for
   // vocabulary passes.
+  // (The children's logits are requested first, so their loads overlap the
+  // fold; N <= 128 < kThreads, one child per thread.)
+  const int cc = 1 + tid;
+  float czv = 0.f, cdv = 0.f;
+  if (sample && cc < N) {
+    const size_t mp = (size_t)b * N + sh.parent[cc];
+    const int x = L.tok[(size_t)b * N + cc];
+    czv = L.z[mp * (size_t)L.V + x];
+    cdv = __bfloat162float(L.dl[mp * (size_t)L.V + x]);
+  }
   fold_all_nodes(L, b, sample, sh);
-  if (sample)
-    for (int c = 1 + tid; c < N; c += kThreads) {
-      const size_t mp = (size_t)b * N + sh.parent[c];
-      const int x = L.tok[(size_t)b * N + c];
-      sh.cz[c] = L.z[mp * (size_t)L.V + x];
-      sh.cd[c] = __bfloat162float(L.dl[mp * (size_t)L.V + x]);
-    }
+  if (sample && cc < N) {
+    sh.cz[cc] = czv;
+    sh.cd[cc] = cdv;
+  }
   __syncthreads();
 
   int par = 0;
@@ -337,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeLaunch
     for (int c = sh.first_child[u]; c >= 0; c = sh.next_sibling[c]) {
       const float zx = sh.cz[c];
       const float dx = sh.cd[c];
-      const float px = exp2f((zx - st.mp) * L.c - st.lsp);
-      const float qx = exp2f((dx - st.mq) * L.c - st.lsq);
+      const float px = ex2((zx - st.mp) * L.c - st.lsp);
+      const float qx = ex2((dx - st.mq) * L.c - st.lsq);
       float f = px;
       for (int j = 1; j <= nrej; ++j) f = fmaxf(0.f, f - qx) * sh.Sinv[j];
       const float r = accept_uniform(L.seed, b, c - 1);
@@ -379,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeLaunch
 
     // ---- draw from the last residual (or p_u) ----
     // The last rejection pass computed exactly these weights: its chunk
-    // sums, prefix and exchanged totals are reused. Otherwise (no child, or
+    // sums and exchanged totals are reused. Otherwise (no child, or
     // the fallback) one pass over p_u.
     const int lev = fallback ? 0 : nrej;
     float total;
@@ -421,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeLaunch
       const float t = before == 3.0e38f ? 3.0e38f : t_all - before;
       const int nch = (hi - lo + kTC - 1) / kTC;
       if (warp == 0) {
+        chunk_prefix(nch, sh);
         int found = -1;
         for (int g = 0; g < nch && found < 0; g += 32) {
           const int k = g + lane;
@@ -471,9 +532,48 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeLaunch
 
 }  // namespace
 
+// How many clusters of kTreeClusterWide CTAs can run at once on this
+// device (0 if the size is not available); cached per device.
+int max_wide_clusters() {
+  static int cache[64];
+  static bool have[64] = {false};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (!have[dev]) {
+    int n = 0;
+    bool refused = cudaFuncSetAttribute(tree_walk_kernel<kTreeClusterWide>,
+                                        cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                        1) != cudaSuccess;
+    if (!refused) {
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(kTreeClusterWide);
+      cfg.blockDim = dim3(kThreads);
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = kTreeClusterWide;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      if (cudaOccupancyMaxActiveClusters(&n, tree_walk_kernel<kTreeClusterWide>, &cfg) !=
+          cudaSuccess) {
+        n = 0;
+        refused = true;
+      }
+    }
+    if (refused) cudaGetLastError();   // the size is not offered: clear that (non-sticky) error
+    cache[dev] = n;
+    have[dev] = true;
+  }
+  return cache[dev];
+}
+
 cudaError_t launch_tree_walk(const TreeLaunch& L, cudaStream_t stream) {
   const bool sample = L.mode == SPECDEC_SAMPLE;
-  const int cw = sample ? kTreeCluster : 1;
+  // Wider clusters halve every vocabulary pass, as long as every
+  // sequence's cluster runs at once.
+  const bool wide = sample && L.B <= max_wide_clusters();
+  const int cw = sample ? (wide ? kTreeClusterWide : kTreeCluster) : 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.B * cw);
   cfg.blockDim = dim3(kThreads);
@@ -487,6 +587,7 @@ cudaError_t launch_tree_walk(const TreeLaunch& L, cudaStream_t stream) {
   attr[1].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
+  if (wide) return cudaLaunchKernelEx(&cfg, tree_walk_kernel<kTreeClusterWide>, L);
   if (sample) return cudaLaunchKernelEx(&cfg, tree_walk_kernel<kTreeCluster>, L);
   return cudaLaunchKernelEx(&cfg, tree_walk_kernel<1>, L);
 }

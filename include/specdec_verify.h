@@ -135,10 +135,17 @@ int specdec_verify_timed(const void* hidden, const void* W_lm, const int32_t* dr
 
 /*
  * End-to-end form: hidden, draft_tokens, draft_logits, out_tokens and
- * n_accepted are HOST pointers (pinned memory gives asynchronous copies);
- * W_lm and the workspace stay on the device. The call copies the inputs in,
- * runs the step and copies the outputs back on `stream`, then synchronises
- * that stream before returning. Workspace: specdec_verify_host_workspace_size().
+ * n_accepted are HOST pointers; W_lm and the workspace stay on the device.
+ * The call moves the inputs in, runs the step and moves the outputs back on
+ * `stream`, then synchronises that stream before returning. When all five
+ * host buffers are pinned and mapped into the GPU's address space (the
+ * runtime reports a device address for each; the two outputs 4-byte
+ * aligned), one kernel
+ * reads the inputs from host memory into the workspace and one writes the
+ * results back (on Grace-Blackwell over NVLink-C2C); otherwise the copy
+ * engines move them (pageable memory is allowed there). Host buffers must
+ * hold the sizes the shape implies. Workspace:
+ * specdec_verify_host_workspace_size().
  */
 size_t specdec_verify_host_workspace_size(int B, int gamma, int d, int V, int dtype, int mode);
 int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t* draft_tokens_host,

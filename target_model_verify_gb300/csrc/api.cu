@@ -526,6 +526,27 @@ size_t specdec_verify_host_workspace_size(int B, int gamma, int d, int V, int dt
   return base + host_staging_bytes(B, gamma, d, V, dtype, mode);
 }
 
+// Device address of a pinned host buffer that is mapped into the GPU's
+// address space, or nullptr (pageable memory, or not mapped).
+void* mapped_device_ptr(const void* host) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host) != cudaSuccess) {
+    cudaGetLastError();   // not a pointer the runtime knows: the copy path handles it
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || a.devicePointer == nullptr) return nullptr;
+  return a.devicePointer;
+}
+
+// One staging segment, in the widest units both ends are aligned to.
+void host_seg(HostSeg& g, const void* src, void* dst, size_t bytes) {
+  const uintptr_t a = (uintptr_t)src | (uintptr_t)dst;
+  g.src = src;
+  g.dst = dst;
+  g.bytes = (long long)bytes;
+  g.unit = a % 16 == 0 ? 16 : a % 4 == 0 ? 4 : 1;
+}
+
 int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t* draft_tokens_host,
                         const void* draft_logits_host, int B, int gamma, int d, int V, int dtype,
                         float temperature, uint64_t seed, int mode, int32_t* out_tokens_host,
@@ -559,20 +580,50 @@ int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t
   p += align_up(M * 4);
   int32_t* d_nacc = reinterpret_cast<int32_t*>(p);
 
-  if (cudaMemcpyAsync(d_hidden, hidden_host, M * d * e, cudaMemcpyHostToDevice, stream) != cudaSuccess ||
-      cudaMemcpyAsync(d_tokens, draft_tokens_host, (size_t)B * gamma * 4, cudaMemcpyHostToDevice,
-                      stream) != cudaSuccess)
-    return SPECDEC_ERR_CUDA;
-  if (sample && cudaMemcpyAsync(d_logits, draft_logits_host, (size_t)B * gamma * V * e,
-                                cudaMemcpyHostToDevice, stream) != cudaSuccess)
-    return SPECDEC_ERR_CUDA;
+  // Mapped pinned host buffers: the GPU gathers the inputs and writes the
+  // results itself (one kernel each way). Otherwise copy-engine transfers.
+  void* m_hidden = mapped_device_ptr(hidden_host);
+  void* m_tokens = mapped_device_ptr(draft_tokens_host);
+  void* m_logits = sample ? mapped_device_ptr(draft_logits_host) : nullptr;
+  void* m_out = mapped_device_ptr(out_tokens_host);
+  void* m_nacc = mapped_device_ptr(n_accepted_host);
+  StageInLaunch S;
+  S.nseg = sample ? 3 : 2;
+  const bool mapped = m_hidden && m_tokens && (!sample || m_logits) && m_out && m_nacc &&
+                     ((uintptr_t)m_out | (uintptr_t)m_nacc) % 4 == 0;
+  if (mapped) {
+    host_seg(S.seg[0], m_hidden, d_hidden, M * d * e);
+    host_seg(S.seg[1], m_tokens, d_tokens, (size_t)B * gamma * 4);
+    if (sample) host_seg(S.seg[2], m_logits, d_logits, (size_t)B * gamma * V * e);
+    if (launch_stage_in(S, num_sms_current(), stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  } else {
+    if (cudaMemcpyAsync(d_hidden, hidden_host, M * d * e, cudaMemcpyHostToDevice, stream) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(d_tokens, draft_tokens_host, (size_t)B * gamma * 4,
+                        cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return SPECDEC_ERR_CUDA;
+    if (sample && cudaMemcpyAsync(d_logits, draft_logits_host, (size_t)B * gamma * V * e,
+                                  cudaMemcpyHostToDevice, stream) != cudaSuccess)
+      return SPECDEC_ERR_CUDA;
+  }
   rc = verify_impl(d_hidden, W_lm, d_tokens, d_logits, B, gamma, d, V, dtype, temperature, seed,
                    mode, d_out, d_nacc, workspace, base, stream_ptr, Extras());
   if (rc != SPECDEC_OK) return rc;
-  if (cudaMemcpyAsync(out_tokens_host, d_out, M * 4, cudaMemcpyDeviceToHost, stream) != cudaSuccess ||
-      cudaMemcpyAsync(n_accepted_host, d_nacc, (size_t)B * 4, cudaMemcpyDeviceToHost, stream) !=
-          cudaSuccess)
+  if (mapped) {
+    StageOutLaunch O;
+    O.src0 = d_out;
+    O.dst0 = static_cast<int32_t*>(m_out);
+    O.n0 = (int)M;
+    O.src1 = d_nacc;
+    O.dst1 = static_cast<int32_t*>(m_nacc);
+    O.n1 = B;
+    if (launch_stage_out(O, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  } else if (cudaMemcpyAsync(out_tokens_host, d_out, M * 4, cudaMemcpyDeviceToHost, stream) !=
+                 cudaSuccess ||
+             cudaMemcpyAsync(n_accepted_host, d_nacc, (size_t)B * 4, cudaMemcpyDeviceToHost,
+                             stream) != cudaSuccess) {
     return SPECDEC_ERR_CUDA;
+  }
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
   return SPECDEC_OK;
 }

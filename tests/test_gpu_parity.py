@@ -206,6 +206,29 @@ def test_host_entry_point_matches_device_entry_point():
     np.testing.assert_array_equal(nacc.numpy(), dev_nacc)
 
 
+@pytest.mark.parametrize("pinned", [True, False])
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+def test_host_entry_point_pinned_and_pageable(pinned, mode):
+    """Pinned buffers take the mapped path (the GPU reads and writes host
+    memory), pageable ones the copy engines; both give the device entry
+    point's results, including shapes whose sizes are not multiples of 16
+    bytes (B * gamma * 4 = 12 bytes of draft tokens)."""
+    import target_model_verify_gb300 as tv
+    w, inp = _gen("llama3_8b_head", 11, B=3, gamma=1, V=3001, d=64)
+    dev_out, dev_nacc, _ = parity.run_library(inp, 1.0, 5, mode, debug=False)
+    host = {k: (v.cpu().pin_memory() if pinned else v.cpu().clone())
+            for k, v in inp.items() if k not in ("W_lm", "sigma")}
+    out_t = torch.full((w.B, w.gamma + 1), -7, dtype=torch.int32)
+    nacc_t = torch.full((w.B,), -7, dtype=torch.int32)
+    if pinned:
+        out_t, nacc_t = out_t.pin_memory(), nacc_t.pin_memory()
+    out, nacc = tv.verify_host(host["hidden"], inp["W_lm"], host["draft_tokens"],
+                               host["draft_logits"] if mode == ov.SAMPLE else None, 1.0, 5, mode,
+                               out_tokens=out_t, n_accepted=nacc_t)
+    np.testing.assert_array_equal(out.numpy(), dev_out)
+    np.testing.assert_array_equal(nacc.numpy(), dev_nacc)
+
+
 def test_prepared_host_step_rereads_its_buffers_each_call():
     """HostStep: bound once; each call re-reads the pinned inputs the caller
     refilled and matches the device entry point for that input and seed."""

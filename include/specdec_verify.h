@@ -141,9 +141,10 @@ int specdec_verify_timed(const void* hidden, const void* W_lm, const int32_t* dr
  * host buffers are pinned and mapped into the GPU's address space (the
  * runtime reports a device address for each; the two outputs 4-byte
  * aligned), one kernel
- * reads the inputs from host memory into the workspace and one writes the
- * results back (on Grace-Blackwell over NVLink-C2C); otherwise the copy
- * engines move them (pageable memory is allowed there). Host buffers must
+ * reads the inputs from host memory into the workspace and the step's
+ * kernels store the results straight into the output buffers (on
+ * Grace-Blackwell over NVLink-C2C); otherwise the copy engines move them
+ * (pageable memory is allowed there). Host buffers must
  * hold the sizes the shape implies. Workspace:
  * specdec_verify_host_workspace_size().
  */

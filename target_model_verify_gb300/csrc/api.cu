@@ -606,24 +606,21 @@ int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t
                                   cudaMemcpyHostToDevice, stream) != cudaSuccess)
       return SPECDEC_ERR_CUDA;
   }
+  // Mapped outputs: the accept and sample kernels write the results straight
+  // into the caller's host buffers (they only ever store to them).
+  if (mapped) {
+    d_out = static_cast<int32_t*>(m_out);
+    d_nacc = static_cast<int32_t*>(m_nacc);
+  }
   rc = verify_impl(d_hidden, W_lm, d_tokens, d_logits, B, gamma, d, V, dtype, temperature, seed,
                    mode, d_out, d_nacc, workspace, base, stream_ptr, Extras());
   if (rc != SPECDEC_OK) return rc;
-  if (mapped) {
-    StageOutLaunch O;
-    O.src0 = d_out;
-    O.dst0 = static_cast<int32_t*>(m_out);
-    O.n0 = (int)M;
-    O.src1 = d_nacc;
-    O.dst1 = static_cast<int32_t*>(m_nacc);
-    O.n1 = B;
-    if (launch_stage_out(O, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
-  } else if (cudaMemcpyAsync(out_tokens_host, d_out, M * 4, cudaMemcpyDeviceToHost, stream) !=
-                 cudaSuccess ||
-             cudaMemcpyAsync(n_accepted_host, d_nacc, (size_t)B * 4, cudaMemcpyDeviceToHost,
-                             stream) != cudaSuccess) {
+  if (!mapped &&
+      (cudaMemcpyAsync(out_tokens_host, d_out, M * 4, cudaMemcpyDeviceToHost, stream) !=
+           cudaSuccess ||
+       cudaMemcpyAsync(n_accepted_host, d_nacc, (size_t)B * 4, cudaMemcpyDeviceToHost, stream) !=
+           cudaSuccess))
     return SPECDEC_ERR_CUDA;
-  }
   if (cudaStreamSynchronize(stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
   return SPECDEC_OK;
 }

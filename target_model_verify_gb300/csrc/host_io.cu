@@ -1,8 +1,9 @@
-// Host <-> device staging for the host entry point. When the step's host
+// Host -> device staging for the host entry point. When the step's host
 // buffers are pinned and mapped into the GPU's address space (on
 // Grace-Blackwell the GPU reaches them over NVLink-C2C), one kernel gathers
-// the step's inputs from host memory into the workspace and one writes the
-// results back, instead of one copy-engine transfer per buffer.
+// the step's inputs from host memory into the workspace instead of one
+// copy-engine transfer per buffer (the results are stored straight into the
+// caller's mapped output buffers by the kernels that produce them).
 #include "kernels.h"
 
 namespace specdec {
@@ -44,12 +45,6 @@ __global__ void __launch_bounds__(256) stage_in_kernel(const StageInLaunch S) {
   }
 }
 
-__global__ void __launch_bounds__(256) stage_out_kernel(const StageOutLaunch S) {
-  grid_dependency_wait();   // the sampler's tokens are complete
-  for (int i = threadIdx.x; i < S.n0; i += blockDim.x) S.dst0[i] = S.src0[i];
-  for (int i = threadIdx.x; i < S.n1; i += blockDim.x) S.dst1[i] = S.src1[i];
-}
-
 }  // namespace
 
 cudaError_t launch_stage_in(const StageInLaunch& S, int num_sms, cudaStream_t stream) {
@@ -61,19 +56,6 @@ cudaError_t launch_stage_in(const StageInLaunch& S, int num_sms, cudaStream_t st
   if (blocks < 1) blocks = 1;
   stage_in_kernel<<<(unsigned)blocks, 256, 0, stream>>>(S);
   return cudaGetLastError();
-}
-
-cudaError_t launch_stage_out(const StageOutLaunch& S, cudaStream_t stream) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(1);
-  cfg.blockDim = dim3(256);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, stage_out_kernel, S);
 }
 
 }  // namespace specdec

@@ -100,8 +100,7 @@ cudaError_t launch_tree_walk(const TreeLaunch& L, cudaStream_t stream);
 
 // Host entry point staging through mapped pinned host memory: segments of
 // `bytes` copied from host to the workspace in `unit`-byte pieces (16, 4 or
-// 1; both ends aligned to it), the remainder byte by byte; then the results
-// back.
+// 1; both ends aligned to it), the remainder byte by byte.
 struct HostSeg {
   const void* src;
   void* dst;
@@ -112,16 +111,7 @@ struct StageInLaunch {
   HostSeg seg[3];
   int nseg;
 };
-struct StageOutLaunch {
-  const int32_t* src0;
-  int32_t* dst0;
-  int n0;
-  const int32_t* src1;
-  int32_t* dst1;
-  int n1;
-};
 cudaError_t launch_stage_in(const StageInLaunch& S, int num_sms, cudaStream_t stream);
-cudaError_t launch_stage_out(const StageOutLaunch& S, cudaStream_t stream);
 
 // Verify-step attention (one layer): split-KV partials and their merge.
 struct AttnLaunch {

@@ -64,6 +64,9 @@ def parse_args(argv=None):
     ap.add_argument("--cluster-head", default=None, metavar="M,K",
                     help="time the drafter's clustered LM head at the Gemma-E2B shape "
                          "(V 262144, d 1536, 2048 clusters of 128): M rows, K kept clusters")
+    ap.add_argument("--gamma-sweep", action="store_true",
+                    help="Gemma-E2B head, gamma in {1,2,3,4,6,8}: mean tokens per step of 4000 "
+                         "sequences with i.i.d. positions against (1 - a^(g+1)) / (1 - a)")
     ap.add_argument("--loop-c", type=float, default=None,
                     help="time the draft->verify loop with a synthetic drafter costing this "
                          "fraction of a target step per draft token (prints its own line)")
@@ -600,6 +603,47 @@ def run_loop(args):
     print(json.dumps(line), flush=True)
 
 
+def run_gamma_sweep(args):
+    """Mean tokens per verify step against the closed form of "推测解码",
+    section 接受率 α, on the Gemma-E2B-shaped head: every position has the same
+    target row p and draft row q, the guesses are fresh draws from q, so
+    acceptances are independent with alpha = sum_v min(p, q) (computed here in
+    fp64 from the same bf16 inputs)."""
+    import target_model_verify_gb300 as tv
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = wl.get("gemma_e2b_head_g1")
+    base = wl.generate(w, args.seed + 21, device=device)
+    W = base["W_lm"]
+    d, V = W.shape[1], W.shape[0]
+    z = base["hidden"][0, 0].double() @ W.double().t()
+    zq = base["draft_logits"][0, 0].double()
+    p, q = torch.softmax(z, 0), torch.softmax(zq, 0)
+    alpha = float(torch.minimum(p, q).sum())
+    g = torch.Generator(device=device)
+    g.manual_seed(args.seed + 40)
+    B, calls = 500, 8
+    for gamma in (1, 2, 3, 4, 6, 8):
+        hidden = base["hidden"][:, :1].expand(B, gamma + 1, d).contiguous()
+        dl = base["draft_logits"][:, :1].expand(B, gamma, V).contiguous()
+        ws = tv.alloc_workspace(B, gamma, d, V, torch.bfloat16, wl.SAMPLE, device=device)
+        n = []
+        for c in range(calls):
+            x = torch.multinomial(q.float(), B * gamma, replacement=True, generator=g)
+            _, nacc = tv.verify(hidden, W, x.view(B, gamma).int(), dl, 1.0, 500 + c, wl.SAMPLE,
+                                workspace=ws)
+            n.append(nacc.double() + 1)
+        n = torch.cat(n)
+        cf = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+        print(json.dumps({"metric": "mean tokens per verify step (i.i.d. positions)",
+                          "gamma": gamma, "alpha": alpha, "measured": float(n.mean()),
+                          "stderr": float(n.std() / n.numel() ** 0.5), "closed_form": cf,
+                          "sequences": n.numel(),
+                          "config": {"workload": "gemma_e2b_head (d 1536, V 262144)",
+                                     "T": 1.0}}), flush=True)
+        del hidden, dl, ws
+
+
 def run_cluster_head(args):
     """The drafter's clustered LM head ("多詞元預測視覺化指南", section
     高效嵌入器): cluster logits, the top-K clusters, their members' logits and
@@ -715,6 +759,9 @@ def main(argv=None):
         return
     if args.cluster_head is not None:
         run_cluster_head(args)
+        return
+    if args.gamma_sweep:
+        run_gamma_sweep(args)
         return
     if args.impl == "reference":
         run_reference(args, world, rank, local)

@@ -120,9 +120,23 @@ def test_llama3_8b_head_batch_sweep(B, mode):
 
 @pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
 def test_head_70b(mode):
+    """70B-shaped head with 5 % near-duplicate hidden rows. Near-duplicate
+    rows give near-identical logit rows, not ties inside a row, so the
+    argmax near-ties (top-2 gap < 1e-3) that actually arise among the
+    checked rows are counted and reported (-s prints them); decisions at
+    such ties are the only ones the parity rule lets differ."""
     w, inp = _gen("head_70b_b32_g7", 2)
     rows = [0, 7, 19, 31]
-    _full_check(w, inp, 4, mode, rows=rows)
+    T = w.temperature
+    out, nacc, dbg = parity.run_library(inp, T, 4, mode)
+    res = parity.run_oracle(inp, T, 4, mode, seq_ids=rows)
+    rep = parity.assert_tokens(out, nacc, res, mode, rows)
+    parity.assert_intermediates(dbg, res, mode, w.B, w.gamma, rows)
+    parity.check_structure(out, nacc, inp["draft_tokens"].cpu().numpy(), w.V)
+    gaps = [ov.greedy_argmax(res.z[k, i])[1] for k in range(len(rows)) for i in range(w.gamma + 1)]
+    ties = sum(g < parity.GREEDY_GAP for g in gaps)
+    print(f"70B head, {len(gaps)} checked rows: {ties} argmax near-ties (gap < {parity.GREEDY_GAP}), "
+          f"smallest gap {min(gaps):.3g}; decisions excused by the margin rule: {rep.excused}")
 
 
 # ------------------------------------------------------------ behaviour --

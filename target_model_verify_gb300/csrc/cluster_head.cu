@@ -119,24 +119,36 @@ __global__ void __launch_bounds__(kThreads) top_clusters_kernel(const ClusterLau
     }
     __syncthreads();
   }
+  __shared__ int s_off[SPECDEC_CLUSTER_MAX_TOP_K + 1], s_row0[SPECDEC_CLUSTER_MAX_TOP_K];
   if (threadIdx.x == 0) {
     int off = 0;
     bool bad = false;
     for (int k = 0; k < L.top_k; ++k) {
       const int c = s_sel[k];
-      const int n = L.starts[c + 1] - L.starts[c];
+      const int r0 = L.starts[c];
+      const int n = L.starts[c + 1] - r0;
       bad |= n < 0 || n > L.max_cluster;
       L.clusters[(size_t)m * L.top_k + k] = c;
       L.offs[(size_t)m * (L.top_k + 1) + k] = off;
+      s_off[k] = off;
+      s_row0[k] = r0;
       off += max(0, min(n, L.max_cluster));
     }
     L.offs[(size_t)m * (L.top_k + 1) + L.top_k] = off;
+    s_off[L.top_k] = off;
     if (bad) set_status(L.status, SPECDEC_ERR_INVALID_ARG);
   }
+  __syncthreads();
+  // The kept members' table rows, in kept order, so the next kernel reads
+  // each member's row with one load (it replaces them by token IDs).
+  for (int k = 0; k < L.top_k; ++k)
+    for (int i = s_off[k] + threadIdx.x; i < s_off[k + 1]; i += kThreads)
+      L.ids[(size_t)m * L.max_members + i] = s_row0[k] + (i - s_off[k]);
 }
 
 // Logits of kept member rows: CTA (block, m) takes members
-// [8 * block, 8 * block + 8) of row m's kept list, one per warp.
+// [8 * block, 8 * block + 8) of row m's kept list, one per warp; each
+// member's table row comes from ids[m, i], which then takes its token ID.
 __global__ void __launch_bounds__(kThreads) member_logits_kernel(const ClusterLaunch L) {
   __shared__ __align__(16) __nv_bfloat16 hs[SPECDEC_CLUSTER_MAX_D];
   grid_launch_dependents();
@@ -151,10 +163,7 @@ __global__ void __launch_bounds__(kThreads) member_logits_kernel(const ClusterLa
     reinterpret_cast<uint4*>(hs)[e] = __ldg(reinterpret_cast<const uint4*>(L.h + (size_t)m * L.d) + e);
   __syncthreads();
   for (int i = i0 + warp; i < min(total, i0 + kMemberBlock); i += kWarps) {
-    int k = 0;
-    while (k + 1 < L.top_k && offs[k + 1] <= i) ++k;
-    const int c = L.clusters[(size_t)m * L.top_k + k];
-    const int r = L.starts[c] + (i - offs[k]);
+    const int r = L.ids[(size_t)m * L.max_members + i];   // table row (written by top_clusters)
     if (r < 0 || r >= L.V) {   // starts outside the table: report, read nothing
       if (lane == 0) set_status(L.status, SPECDEC_ERR_INVALID_ARG);
       continue;
@@ -169,8 +178,9 @@ __global__ void __launch_bounds__(kThreads) member_logits_kernel(const ClusterLa
   }
 }
 
-// Draft token of row m: members sorted by token ID (bitonic, shared memory),
-// then the greedy argmax or the inverse CDF of softmax(z / T).
+// Draft token of row m: members put in token-ID order in shared memory (by
+// counting ranks up to 256 members, else a bitonic sort), then the greedy
+// argmax or the inverse CDF of softmax(z / T).
 __global__ void __launch_bounds__(kThreads) draw_kernel(const ClusterLaunch L) {
   extern __shared__ __align__(16) uint8_t smem_d[];
   int* sid = reinterpret_cast<int*>(smem_d);
@@ -183,6 +193,29 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const ClusterLaunch L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = L.offs[(size_t)m * (L.top_k + 1) + L.top_k];
   const int n = L.sort_n;   // power of two >= max_members
+  if (total <= kThreads) {
+    // One member per thread: its place in token-ID order is the number of
+    // members before it (lower ID, or equal ID and lower index), counted
+    // against all IDs staged in shared memory (the z area holds them).
+    int* sin = reinterpret_cast<int*>(sz);
+    const int t = threadIdx.x;
+    const int my_id = t < total ? L.ids[(size_t)m * L.max_members + t] : 0;
+    const float my_z = t < total ? L.z[(size_t)m * L.max_members + t] : 0.f;
+    if (t < total) sin[t] = my_id;
+    __syncthreads();
+    int rank = 0;
+    if (t < total)
+      for (int j = 0; j < total; ++j) {
+        const int o = sin[j];
+        rank += (o < my_id || (o == my_id && j < t)) ? 1 : 0;
+      }
+    __syncthreads();
+    if (t < total) {
+      sid[rank] = my_id;
+      sz[rank] = my_z;
+    }
+    __syncthreads();
+  } else {
   for (int i = threadIdx.x; i < n; i += kThreads) {
     const bool in = i < total;
     sid[i] = in ? L.ids[(size_t)m * L.max_members + i] : 0x7fffffff;
@@ -208,6 +241,7 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const ClusterLaunch L) {
       }
       __syncthreads();
     }
+  }
   // max logit (and its lowest token ID: members are in token-ID order)
   float bv = -INFINITY;
   int bi = 0x7fffffff;

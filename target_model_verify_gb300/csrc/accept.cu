@@ -33,6 +33,7 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
 
   grid_dependency_wait();      // the LM-head kernel's records are complete
   grid_launch_dependents();    // the sampler may start launching
+  if (b == 0 && threadIdx.x == 0) *a.calls += 1;   // the LM head of this call is done
 
   // The drafted tokens' logits do not depend on the folds: warp 0 loads
   // them first, so their latency overlaps the record loads.

@@ -2,6 +2,7 @@
 // and the stream-ordered launch sequence
 //   LM-head scoring (+ softmax/argmax partials)  ->  acceptance scan
 //   ->  residual / bonus draw (sampling mode only).
+#include <cstddef>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -156,6 +157,13 @@ bool encode_kv_cache(CUtensorMap* map, const void* base, int B, int Lmax, int Hk
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The call count in the header that starts every workspace (its status
+// word is the header's first field).
+unsigned long long* header_calls(int* status) {
+  return reinterpret_cast<unsigned long long*>(reinterpret_cast<char*>(status) +
+                                               offsetof(WsHeader, calls));
+}
+
 struct Extras {
   float* logits_out = nullptr;
   float* lse_p = nullptr;
@@ -199,6 +207,7 @@ int lmhead_stage_bf16(const void* hidden, const void* W, int M, int d, int V, co
   L.fix = reinterpret_cast<float*>(ws + off_fix);
   L.fix_tickets = reinterpret_cast<unsigned long long*>(ws + off_tickets);
   L.epoch = epoch;
+  L.calls = header_calls(status);
   L.max_clusters = max_clusters;
   L.withhold_loads = 0;
   L.ep = ep;
@@ -297,6 +306,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   A.sel = sel;
   A.counters = counters;
   A.status = status;
+  A.calls = header_calls(status);
   A.lse_p = ex.lse_p;
   A.lse_q = ex.lse_q;
   A.p_x = ex.p_x;
@@ -673,6 +683,7 @@ int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void*
   L.fix = reinterpret_cast<float*>(ws + pl.off_fix);
   L.fix_tickets = reinterpret_cast<unsigned long long*>(ws + pl.off_tickets);
   L.epoch = next_call_epoch();
+  L.calls = header_calls(L.status);
   L.max_clusters = 0;
   L.withhold_loads = 1;
   L.ep = ep;
@@ -781,6 +792,7 @@ int specdec_verify_tree_timed(const void* hidden, const void* W_lm, const int32_
   T.out_nodes = out_nodes;
   T.n_accepted = n_accepted;
   T.status = status;
+  T.calls = header_calls(status);
   return launch_tree_walk(T, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
 }
 

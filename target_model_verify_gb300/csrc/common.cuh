@@ -50,8 +50,22 @@ struct SelectedRow {
 // follow it at fixed offsets computed on the host.
 struct WsHeader {
   int status;
-  int pad[63];
+  int pad0;
+  // Calls that have used this workspace (any initial value): the kernel
+  // after the LM head adds one. Mixed into the LM head's fix-up tag, it keeps
+  // tags distinct when a captured CUDA graph replays the same launch.
+  unsigned long long calls;
+  int pad[60];
 };
+static_assert(sizeof(WsHeader) == 256, "workspace header");
+
+// Fix-up tag of one LM-head call: the host's per-launch tag mixed with the
+// workspace's call count.
+__device__ __forceinline__ unsigned long long call_tag(unsigned long long epoch,
+                                                       const unsigned long long* calls) {
+  return epoch ^ (*reinterpret_cast<const volatile unsigned long long*>(calls) *
+                  0x9E3779B97F4A7C15ull);
+}
 
 // ------------------------------------------------------------- status --
 

@@ -21,6 +21,7 @@ struct TcLaunch {
   float* fix;                    // stream-K fix-up slots (tc_fix_floats floats)
   unsigned long long* fix_tickets;   // kFixSlots tags, any initial contents
   unsigned long long epoch;      // per-call tag (next_call_epoch)
+  const unsigned long long* calls;   // the workspace header's call count
   int max_clusters;              // co-resident clusters of the launch shape (0: unknown)
   int withhold_loads;            // self-test of the bounded waits (normally 0)
   EpiParams ep;
@@ -49,6 +50,7 @@ struct AcceptLaunch {
   SelectedRow* sel;
   int* counters;
   int* status;
+  unsigned long long* calls;     // the workspace header's call count (one added per call)
   float* lse_p;
   float* lse_q;
   float* p_x;
@@ -95,6 +97,7 @@ struct TreeLaunch {
   int32_t* out_nodes;            // [B, N]
   int32_t* n_accepted;           // [B]
   int* status;
+  unsigned long long* calls;     // the workspace header's call count (one added per call)
 };
 cudaError_t launch_tree_walk(const TreeLaunch& L, cudaStream_t stream);
 

@@ -103,7 +103,8 @@ struct TcParams {
   int* status;
   float* fix;                    // [slots * 2][BT * 128] partial accumulators
   unsigned long long* fix_tickets;   // [slots]: epoch of the last part to arrive
-  unsigned long long epoch;      // this call's tag (never repeats within a process)
+  unsigned long long epoch;      // this launch's host tag (never repeats within a process)
+  const unsigned long long* calls;   // the workspace's call count, mixed into the tag
   int withhold_loads;            // self-test: issue no loads, so the first wait runs out
   int z_tma;                     // row owner: logits leave through bulk tensor stores
   EpiParams ep;
@@ -286,6 +287,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the previous kernel; global memory is touched only after this wait.
   grid_dependency_wait();
   if (blockIdx.x == 0 && threadIdx.x == 0) *(volatile int*)p.status = SPECDEC_OK;
+  // This call's fix-up tag; the call count only changes after this kernel.
+  const unsigned long long tag = call_tag(p.epoch, p.calls);
   tc_fence_before();
   __syncthreads();
   if (pair) cluster_sync_all();   // the partner's barriers exist before any remote arrive
@@ -561,9 +564,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         named_bar_sync(1, kEpiThreads);
         if (threadIdx.x == 64) {
-          const unsigned long long prev = atomicExch(p.fix_tickets + slot, p.epoch);
+          const unsigned long long prev = atomicExch(p.fix_tickets + slot, tag);
           __threadfence();
-          *epi_flag = prev == p.epoch ? 1 : 0;
+          *epi_flag = prev == tag ? 1 : 0;
         }
         named_bar_sync(1, kEpiThreads);
         finish = *epi_flag != 0;
@@ -725,10 +728,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __threadfence();
         named_bar_sync(1, kEpiThreads);
         if (epi_tid == 0) {
-          // The part that finds this call's epoch already there arrives second.
-          const unsigned long long prev = atomicExch(p.fix_tickets + slot, p.epoch);
+          // The part that finds this call's tag already there arrives second.
+          const unsigned long long prev = atomicExch(p.fix_tickets + slot, tag);
           __threadfence();
-          *epi_flag = prev == p.epoch ? 1 : 0;
+          *epi_flag = prev == tag ? 1 : 0;
         }
         named_bar_sync(1, kEpiThreads);
         finish = *epi_flag != 0;
@@ -940,6 +943,7 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   p.fix = L.fix;
   p.fix_tickets = L.fix_tickets;
   p.epoch = L.epoch;
+  p.calls = L.calls;
   p.withhold_loads = L.withhold_loads;
   p.z_tma = (g.rowown && L.tmap_z != nullptr) ? 1 : 0;
   p.ep = L.ep;

@@ -330,6 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1) tree_walk_kernel(const TreeLaunch
   }
   __syncthreads();
   grid_dependency_wait();   // the LM-head kernel's records, logits and q records are complete
+  if (blockIdx.x == 0 && threadIdx.x == 0) *L.calls += 1;   // the LM head of this call is done
   const int prior = *(volatile int*)L.status;
   bool bad = false;
   for (int n = 1 + tid; n < N; n += kThreads) {

@@ -394,3 +394,53 @@ def test_gemma_tokens_per_step_follow_the_closed_form(gamma):
     var = float((pk * vals ** 2).sum() - mean ** 2)
     assert 0.5 < alpha < 0.8, alpha
     assert abs(n.mean() - mean) < 5 * np.sqrt(var / n.size), (n.mean(), mean, alpha)
+
+
+def test_verify_step_replays_in_a_cuda_graph():
+    """The step captured once in a CUDA graph gives, on every replay, exactly
+    what the same call gives when launched directly -- logits, records and
+    tokens. The Llama-3-8B head splits vocabulary tiles between CTAs
+    (stream-K), and every replay repeats the same launch parameters, so this
+    also checks that a split tile is never finished from the previous
+    replay's partial (the workspace's call count keeps the fix-up tags
+    distinct)."""
+    import target_model_verify_gb300 as tv
+    w, inp = _gen("llama3_8b_head", 13)
+    B, g1, V = w.B, w.gamma + 1, w.V
+    ws = tv.alloc_workspace(B, w.gamma, w.d, V, torch.bfloat16, ov.SAMPLE, device=DEV)
+
+    def buffers():
+        return (torch.empty(B, g1, dtype=torch.int32, device=DEV),
+                torch.empty(B, dtype=torch.int32, device=DEV),
+                {"logits": torch.empty(B * g1, V, device=DEV),
+                 "lse_p": torch.empty(B * g1, device=DEV),
+                 "lse_q": torch.empty(B * w.gamma, device=DEV),
+                 "p_x": torch.empty(B * w.gamma, device=DEV),
+                 "q_x": torch.empty(B * w.gamma, device=DEV)})
+
+    def step(out, nacc, dbg):
+        tv.verify(inp["hidden"], inp["W_lm"], inp["draft_tokens"], inp["draft_logits"], 1.0, 21,
+                  ov.SAMPLE, out_tokens=out, n_accepted=nacc, workspace=ws, debug=dbg)
+
+    ref = buffers()
+    step(*ref)
+    torch.cuda.synchronize()
+    got = buffers()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(*got)                      # warm-up on the capture's stream kind
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(*got)
+    for _ in range(3):
+        for t in (got[0], got[1], *got[2].values()):
+            t.fill_(-7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert tv.read_status(ws) == 0
+        assert torch.equal(got[0], ref[0]) and torch.equal(got[1], ref[1])
+        for k in ref[2]:
+            assert torch.equal(got[2][k], ref[2][k]), k

@@ -195,3 +195,44 @@ def test_tree_first_token_law_on_the_gpu():
     chi2 = float((((counts[keep] - exp[keep]) ** 2) / exp[keep]).sum())
     dof = int(keep.sum()) - 1
     assert chi2 < dof + 6 * np.sqrt(2 * dof), (chi2, dof)
+
+
+def test_tree_step_replays_in_a_cuda_graph():
+    """The 26-node tree step on the Llama-3-8B head, captured once in a CUDA
+    graph: every replay writes the direct call's tokens, nodes and counts
+    (split LM-head tiles get a fresh fix-up tag each replay)."""
+    import target_model_verify_gb300 as tv
+    w = wl.get("llama3_8b_head_tree26_b8")
+    inp = wl.generate_tree(w, 4, device=DEV)
+    B, N = w.B, w.N
+    ws = tv.alloc_tree_workspace(B, N, w.d, w.V, torch.bfloat16, ov.SAMPLE, device=DEV)
+
+    def bufs():
+        return tuple(torch.empty(*s, dtype=torch.int32, device=DEV) for s in ((B, N), (B, N), (B,)))
+
+    def step(o, n, a):
+        tv.verify_tree(inp["hidden"], inp["W_lm"], inp["parent"], inp["node_tokens"],
+                       inp["draft_logits"], w.temperature, 17, ov.SAMPLE, out_tokens=o,
+                       out_nodes=n, n_accepted=a, workspace=ws)
+
+    ref = bufs()
+    step(*ref)
+    torch.cuda.synchronize()
+    got = bufs()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        step(*got)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(*got)
+    for _ in range(3):
+        for t in got:
+            t.fill_(-7)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert tv.read_status(ws) == 0
+        for a, b in zip(got, ref):
+            assert torch.equal(a, b)

@@ -76,15 +76,24 @@ def test_tiny_fp32_sampling(seed):
     (7, 3, 8, 300, 1.0),        # d = 8: one zero-padded k-slice
     (16, 4, 200, 2049, 0.9),    # M = 80: cluster pairs with 2-D boxes (d % 64 != 0), odd tile count
     (16, 4, 128, 1920, 1.1),    # M = 80: cluster pairs with 3-D boxes, 15 tiles (one past the end)
-    (40, 4, 64, 3000, 1.0),     # M = 200: one token tile of 208, clusters, q from its own kernel
+    (40, 4, 64, 3000, 1.0),     # M = 200: one token tile of 208, clusters, q streamed whole
     (64, 3, 128, 2049, 0.9),    # M = 256: tokens on the MMA's M side, stream-K, V % 4 != 0
     (64, 3, 200, 1000, 1.0),    # M = 256, tokens on M with 2-D boxes and a ragged k-slice
     (100, 4, 64, 3001, 1.0),    # M = 500: two token tiles of 256 on M, the last one partial
     (128, 3, 192, 1024, 1.2),   # M = 512: two full token tiles on M, vector logit stores
+    (1024, 4, 64, 1000, 1.0),   # M = 5120: twenty token tiles, 1,024 sampler sequences
 ])
 def test_bf16_small_shapes(mode, B, gamma, d, V, T):
     w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, temperature=T, sigma=0.4)
     inp = wl.generate(w, 11 + B, device=DEV)
+    _full_check(w, inp, 5, mode)
+
+
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+def test_largest_vocabulary(mode):
+    """V one below the largest vocabulary the library takes (2^22 - 1:
+    1,024 sampler chunks, the last one ragged; 32,768 vocabulary tiles)."""
+    w, inp = _gen("llama3_8b_head", 3, B=1, gamma=2, d=64, V=(1 << 22) - 1, w_std=0.3)
     _full_check(w, inp, 5, mode)
 
 

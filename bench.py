@@ -679,11 +679,34 @@ def run_cluster_head(args):
         raise RuntimeError("device status after the clustered head")
     us = e0.elapsed_time(e1) * 1e3 / Kst
     bytes_read = n_c * d * 2 + M * K * size * d * 2 + M * d * 2
+    peaks, kind = load_peaks()
+    cpu = None
+    if not args.no_cpu_baseline:
+        # The fp64 oracle on the same rows (the tables converted once,
+        # outside the timing), for ~10 s.
+        from oracle import cluster_head as och
+        f64 = lambda t: t.float().cpu().double().numpy()
+        hs, Es, Ws = f64(h), f64(E), f64(W)
+        st_, tr_ = starts.cpu().numpy(), tor.cpu().numpy()
+        n, t0 = 0, time.perf_counter()
+        while n < 1 or time.perf_counter() - t0 < CPU_BASELINE_SECONDS:
+            och.cluster_head(hs, Es, Ws, st_, tr_, K, 1.0, n, wl.SAMPLE)
+            n += 1
+        cpu = {"value": (time.perf_counter() - t0) / n * 1e6, "unit": "us",
+               "cores": host_cores(), "kind": "oracle",
+               "sample": f"{n} full calls of the fp64 NumPy oracle (tables converted to fp64 "
+                         f"once outside the timing)"}
     line = {
         "metric": "drafter clustered LM head, one call", "value": us, "unit": "us",
         "higher_is_better": False, "steps": Kst, "warmup": Wm,
         "bytes_read": bytes_read, "full_head_bytes": V * d * 2,
         "achieved_gbs": bytes_read / (us * 1e-6) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": bytes_read / (us * 1e-6) / 1e9,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": bytes_read / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                     "algorithmic_bytes": bytes_read, "kernel": "cluster head (4 kernels)",
+                     "peak_source": f"{kind} (MEASURED_PEAKS.json)"},
+        "cpu_baseline": cpu,
         "config": {"M": M, "top_k": K, "V": V, "d": d, "clusters": n_c, "cluster_size": size,
                    "mode": "sample", "l2": "cluster table and kept rows fit in L2 (latency-bound)"},
     }
@@ -727,6 +750,22 @@ def run_attention(args):
     if tv.read_status(ws) != 0:
         raise RuntimeError("device status after attention")
     us = e0.elapsed_time(e1) * 1e3 / K
+    cpu = None
+    if not args.no_cpu_baseline:
+        # The fp64 oracle on one sequence at a time (inputs converted once),
+        # as many as ~10 s allow, scaled to calls of all B sequences.
+        from oracle import attention as oa
+        qs = q[:1].float().cpu().double().numpy()
+        ks = k[:1].float().cpu().double().numpy()
+        vs = v[:1].float().cpu().double().numpy()
+        ls = lens[:1].cpu().numpy()
+        n, t0 = 0, time.perf_counter()
+        while n < 1 or time.perf_counter() - t0 < CPU_BASELINE_SECONDS:
+            oa.verify_attention(qs, ks, vs, ls)
+            n += 1
+        per_seq = (time.perf_counter() - t0) / n
+        cpu = {"value": per_seq * B * 1e6, "unit": "us", "cores": host_cores(), "kind": "oracle",
+               "sample": f"{n} single-sequence calls of the fp64 NumPy oracle, scaled to B={B}"}
     kv_bytes = 2 * B * L * Hkv * D * 2
     bytes_alg = kv_bytes + q.numel() * 2 + out.numel() * 4
     peaks, kind = load_peaks()
@@ -738,6 +777,7 @@ def run_attention(args):
                      "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
                      "algorithmic_bytes": bytes_alg, "kernel": "attn_split_kernel",
                      "peak_source": f"{kind} (MEASURED_PEAKS.json)"},
+        "cpu_baseline": cpu,
         "config": {"B": B, "cached_tokens": L, "new_positions": n_new, "Hq": Hq, "Hkv": Hkv,
                    "D": D, "l2": "KV cache larger than L2 per call" if kv_bytes > 129e6 else
                    "KV cache smaller than L2"},

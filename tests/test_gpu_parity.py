@@ -82,6 +82,8 @@ def test_tiny_fp32_sampling(seed):
     (100, 4, 64, 3001, 1.0),    # M = 500: two token tiles of 256 on M, the last one partial
     (128, 3, 192, 1024, 1.2),   # M = 512: two full token tiles on M, vector logit stores
     (1024, 4, 64, 1000, 1.0),   # M = 5120: twenty token tiles, 1,024 sampler sequences
+    (8, 4, 128, 1500, 0.05),    # cold: logits / T spread over hundreds, p nearly one-hot
+    (8, 4, 128, 1500, 20.0),    # hot: p and q nearly uniform
 ])
 def test_bf16_small_shapes(mode, B, gamma, d, V, T):
     w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, temperature=T, sigma=0.4)

@@ -26,6 +26,13 @@
 // peer's epilogue releases an accumulator by arriving on the leader's
 // barrier. K = 1 elsewhere.
 //
+// Row owner: a pair with token tiles of 256 rows swaps the operands back,
+// tokens on the MMA's M side (A = 128 token rows per CTA, B = 128 W rows
+// per CTA), so tensor-memory lane = token row. Each epilogue thread then
+// owns one token row and keeps its softmax and argmax partials in
+// registers (no shuffles), and the logits leave through bulk tensor stores
+// of 32 x 32 fp32 tiles staged in shared memory.
+//
 // Scheduling, one persistent CTA per SM, in cluster units (K neighbouring
 // vocabulary tiles x one token tile; CTA rank r of the cluster takes tile
 // K*unit + r):
@@ -35,7 +42,11 @@
 //     leaves each CTA a partial accumulator; both write theirs to a fix-up
 //     slot and take an atomic ticket, and the second to arrive adds the two
 //     and runs the epilogue (nobody waits). Each CTA folds the softmax
-//     partials of all its tiles into one record per token row.
+//     partials of all its tiles into one record per token row. Tickets
+//     hold a per-call tag: the host's launch epoch mixed with the
+//     workspace's call count, which the kernel after this one advances, so
+//     stale tickets never match, not even when a captured CUDA graph replays
+//     the launch with identical parameters.
 //   * several token tiles: units dealt round-robin with the token tile
 //     fastest, so the clusters that share W tiles run together and read
 //     them once from HBM and the rest from L2; one record per (row, tile).
@@ -52,6 +63,10 @@
 //              (8 rows in flight per warp) and reduce their softmax
 //              partials for q, off the epilogue's critical path. The CTA
 //              holding a tile's first k-step scores that tile's draft rows.
+//              With more than 16 draft rows, warps 10-12 instead stream
+//              whole (draft row, 8192-column) items dealt across the grid,
+//              one record each (warp 13 shares the MMA issuer's scheduler
+//              and stays out).
 // Every wait is bounded (1 s); a timeout records SPECDEC_ERR_TIMEOUT, stops
 // the other roles, waits for copies and MMAs already issued, frees tensor
 // memory and returns (a cluster partner's waits then run out as well, so

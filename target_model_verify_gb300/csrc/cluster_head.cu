@@ -4,7 +4,7 @@
 // draft token from the softmax over those members.
 //
 // Four small kernels, each a programmatic dependent of the one before:
-//   cluster_logits   y[m, c] = h_m . E_c          one warp per cluster
+//   cluster_logits   y[m, c] = h_m . E_c          one warp per cluster, E_c in registers
 //   top_clusters     the k largest y per row      one CTA per row
 //   member_logits    z = h_m . W_r for kept rows  one kept row per warp
 //   draw             argmax, or the inverse CDF of softmax(z / T) in token-ID
@@ -19,6 +19,10 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerChunk = 16;   // hidden rows staged in shared memory at once
+constexpr int kRowGroup = 8;        // hidden rows a warp dots with its cluster row together
+constexpr int kRankPer = 1;         // members per thread when the draw orders them by counting
+constexpr int kMaxPieces = SPECDEC_CLUSTER_MAX_D / 256;   // 16-byte pieces of a row per lane
+static_assert(kMaxPieces == 16, "cluster_logits instantiations cover d up to 4096");
 constexpr int kMemberBlock = kWarps;   // member rows per CTA of member_logits: one per warp
 constexpr int kDotDepth = 4;            // 16-byte loads a lane keeps in flight in warp_dot
 
@@ -56,6 +60,8 @@ __device__ __forceinline__ float warp_dot(const __nv_bfloat16* __restrict__ row,
   return warp_sum(acc);
 }
 
+// kPieces: 16-byte pieces per lane the instantiation holds (d <= kPieces * 256).
+template <int kPieces>
 __global__ void __launch_bounds__(kThreads) cluster_logits_kernel(const ClusterLaunch L) {
   extern __shared__ __align__(16) uint8_t smem_h[];
   __nv_bfloat16* hs = reinterpret_cast<__nv_bfloat16*>(smem_h);
@@ -66,17 +72,62 @@ __global__ void __launch_bounds__(kThreads) cluster_logits_kernel(const ClusterL
   if (blockIdx.x == 0 && threadIdx.x == 0) *L.status = SPECDEC_OK;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int c = blockIdx.x * kWarps + warp;
+  // With kRowGroup rows or more, the warp's cluster embedding stays in
+  // registers (16-byte piece k of the row at lane * 8 + k * 256) and hidden
+  // rows are dotted with it kRowGroup at a time, so their reductions
+  // overlap.
+  const int npc = L.d / 256 + ((lane * 8) < (L.d % 256) ? 1 : 0);   // pieces this lane holds
+  uint4 e[kPieces];
+#pragma unroll
+  for (int k = 0; k < kPieces; ++k)
+    e[k] = (c < L.n_c && k < npc && L.M >= kRowGroup)
+               ? __ldg(reinterpret_cast<const uint4*>(L.E + (size_t)c * L.d + lane * 8 + k * 256))
+               : make_uint4(0u, 0u, 0u, 0u);
   for (int m0 = 0; m0 < L.M; m0 += kRowsPerChunk) {
     const int nm = min(kRowsPerChunk, L.M - m0);
     __syncthreads();
-    for (int e = threadIdx.x; e < nm * L.d / 8; e += kThreads)
-      reinterpret_cast<uint4*>(hs)[e] = __ldg(reinterpret_cast<const uint4*>(L.h + (size_t)m0 * L.d) + e);
+    for (int q = threadIdx.x; q < nm * L.d / 8; q += kThreads)
+      reinterpret_cast<uint4*>(hs)[q] = __ldg(reinterpret_cast<const uint4*>(L.h + (size_t)m0 * L.d) + q);
     __syncthreads();
-    if (c < L.n_c)
+    if (c >= L.n_c) continue;
+    if (L.M < kRowGroup) {   // few rows: one dot at a time, the row streamed from L2
       for (int m = 0; m < nm; ++m) {
         const float y = warp_dot(L.E + (size_t)c * L.d, hs + (size_t)m * L.d, L.d);
         if (lane == 0) L.y[(size_t)(m0 + m) * L.n_c + c] = y;
       }
+      continue;
+    }
+    for (int g0 = 0; g0 < nm; g0 += kRowGroup) {
+      float acc[kRowGroup];
+#pragma unroll
+      for (int j = 0; j < kRowGroup; ++j) acc[j] = 0.f;
+#pragma unroll
+      for (int k = 0; k < kPieces; ++k) {
+        if (k >= npc) break;
+        const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&e[k]);
+#pragma unroll
+        for (int j = 0; j < kRowGroup; ++j) {
+          if (g0 + j >= nm) break;
+          const uint4 b = *reinterpret_cast<const uint4*>(hs + (size_t)(g0 + j) * L.d + lane * 8 + k * 256);
+          const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&b);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float2 x = __bfloat1622float2(pa[q]);
+            const float2 y = __bfloat1622float2(pb[q]);
+            acc[j] = fmaf(x.x, y.x, acc[j]);
+            acc[j] = fmaf(x.y, y.y, acc[j]);
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1)
+#pragma unroll
+        for (int j = 0; j < kRowGroup; ++j) acc[j] += __shfl_xor_sync(0xffffffffu, acc[j], o);
+      if (lane == 0)
+#pragma unroll
+        for (int j = 0; j < kRowGroup; ++j)
+          if (g0 + j < nm) L.y[(size_t)(m0 + g0 + j) * L.n_c + c] = acc[j];
+    }
   }
 }
 
@@ -193,26 +244,39 @@ __global__ void __launch_bounds__(kThreads) draw_kernel(const ClusterLaunch L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = L.offs[(size_t)m * (L.top_k + 1) + L.top_k];
   const int n = L.sort_n;   // power of two >= max_members
-  if (total <= kThreads) {
-    // One member per thread: its place in token-ID order is the number of
-    // members before it (lower ID, or equal ID and lower index), counted
-    // against all IDs staged in shared memory (the z area holds them).
+  if (total <= kRankPer * kThreads) {
+    // Up to kRankPer member(s) per thread: a member's place in token-ID order
+    // is the number of members before it (lower ID, or equal ID and lower
+    // index), counted against all IDs staged in shared memory (the z area
+    // holds them).
     int* sin = reinterpret_cast<int*>(sz);
-    const int t = threadIdx.x;
-    const int my_id = t < total ? L.ids[(size_t)m * L.max_members + t] : 0;
-    const float my_z = t < total ? L.z[(size_t)m * L.max_members + t] : 0.f;
-    if (t < total) sin[t] = my_id;
+    int my_id[kRankPer], rank[kRankPer];
+    float my_z[kRankPer];
+#pragma unroll
+    for (int u = 0; u < kRankPer; ++u) {
+      const int t = threadIdx.x + u * kThreads;
+      my_id[u] = t < total ? L.ids[(size_t)m * L.max_members + t] : 0;
+      my_z[u] = t < total ? L.z[(size_t)m * L.max_members + t] : 0.f;
+      rank[u] = 0;
+      if (t < total) sin[t] = my_id[u];
+    }
     __syncthreads();
-    int rank = 0;
-    if (t < total)
-      for (int j = 0; j < total; ++j) {
-        const int o = sin[j];
-        rank += (o < my_id || (o == my_id && j < t)) ? 1 : 0;
+    for (int j = 0; j < total; ++j) {
+      const int o = sin[j];
+#pragma unroll
+      for (int u = 0; u < kRankPer; ++u) {
+        const int t = threadIdx.x + u * kThreads;
+        rank[u] += (o < my_id[u] || (o == my_id[u] && j < t)) ? 1 : 0;
       }
+    }
     __syncthreads();
-    if (t < total) {
-      sid[rank] = my_id;
-      sz[rank] = my_z;
+#pragma unroll
+    for (int u = 0; u < kRankPer; ++u) {
+      const int t = threadIdx.x + u * kThreads;
+      if (t < total) {
+        sid[rank[u]] = my_id[u];
+        sz[rank[u]] = my_z[u];
+      }
     }
     __syncthreads();
   } else {
@@ -337,7 +401,10 @@ cudaError_t launch_cluster_head(const ClusterLaunch& L, cudaStream_t stream) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64 || !set[dev]) {
-    e = cudaFuncSetAttribute(cluster_logits_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(cluster_logits_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kRowsPerChunk * SPECDEC_CLUSTER_MAX_D * 2);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(cluster_logits_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              kRowsPerChunk * SPECDEC_CLUSTER_MAX_D * 2);
     if (e != cudaSuccess) return e;
     e = cudaFuncSetAttribute(draw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -345,7 +412,9 @@ cudaError_t launch_cluster_head(const ClusterLaunch& L, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64) set[dev] = 1;
   }
-  e = launch_pdl((const void*)cluster_logits_kernel, dim3((L.n_c + kWarps - 1) / kWarps),
+  const void* logits_fn = L.d <= 8 * 256 ? (const void*)cluster_logits_kernel<8>
+                                         : (const void*)cluster_logits_kernel<16>;
+  e = launch_pdl(logits_fn, dim3((L.n_c + kWarps - 1) / kWarps),
                  dim3(kThreads), smem1, L, stream);
   if (e != cudaSuccess) return e;
   e = launch_pdl((const void*)top_clusters_kernel, dim3(L.M), dim3(kThreads), 0, L, stream);

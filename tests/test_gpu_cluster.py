@@ -81,6 +81,14 @@ def test_cluster_head_gemma_shape(top_k):
     _compare(x, top_k, 1.0, 3, ov.SAMPLE)
 
 
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+def test_cluster_head_more_than_1024_kept_tokens(mode):
+    """2,000 kept tokens per row: the draw orders them with the bitonic sort
+    (up to 256 it counts ranks)."""
+    x = _head(12, 4, 64, 6000, 12, ragged=False)
+    _compare(x, 4, 1.0, 9, mode, position=1)
+
+
 def test_cluster_head_draws_follow_the_uniforms():
     """Different positions and seeds give the oracle's different draws."""
     x = _head(9, 16, 64, 1000, 8)

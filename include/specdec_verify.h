@@ -294,9 +294,10 @@ int specdec_cluster_head(const void* hidden, const void* cluster_emb, const void
 
 /*
  * Reads the device status word of a workspace after synchronising `stream`:
- * SPECDEC_OK, SPECDEC_ERR_TIMEOUT or SPECDEC_ERR_TOKEN_RANGE of the last
- * call that used it. *status receives the value; the return code reports
- * the read itself.
+ * SPECDEC_OK, SPECDEC_ERR_TIMEOUT, SPECDEC_ERR_TOKEN_RANGE (verify and tree
+ * steps) or SPECDEC_ERR_INVALID_ARG (attention lengths, clustered-head
+ * tables) of the last call that used it. *status receives the value; the
+ * return code reports the read itself.
  */
 int specdec_read_status(const void* workspace, void* stream, int32_t* status);
 

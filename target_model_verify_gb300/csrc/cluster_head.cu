@@ -3,8 +3,9 @@
 // top-k clusters, compute token logits for their members only, and draw the
 // draft token from the softmax over those members.
 //
-// Four small kernels, each a programmatic dependent of the one before:
-//   cluster_logits   y[m, c] = h_m . E_c          one warp per cluster, E_c in registers
+// Four small kernels, each a programmatic dependent of the one before
+// (three for one kept cluster and M <= 8: the member kernel then selects it):
+//   cluster_logits   y[m, c] = h_m . E_c          one warp per cluster
 //   top_clusters     the k largest y per row      one CTA per row
 //   member_logits    z = h_m . W_r for kept rows  one kept row per warp
 //   draw             argmax, or the inverse CDF of softmax(z / T) in token-ID
@@ -21,6 +22,7 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRowsPerChunk = 16;   // hidden rows staged in shared memory at once
 constexpr int kRowGroup = 8;        // hidden rows a warp dots with its cluster row together
 constexpr int kRankPer = 1;         // members per thread when the draw orders them by counting
+constexpr int kFuseRows = 8;        // rows up to which (one kept cluster) the member kernel selects it
 constexpr int kMaxPieces = SPECDEC_CLUSTER_MAX_D / 256;   // 16-byte pieces of a row per lane
 static_assert(kMaxPieces == 16, "cluster_logits instantiations cover d up to 4096");
 constexpr int kMemberBlock = kWarps;   // member rows per CTA of member_logits: one per warp
@@ -131,15 +133,15 @@ __global__ void __launch_bounds__(kThreads) cluster_logits_kernel(const ClusterL
   }
 }
 
-// The k largest cluster logits of row m (ties to the lower index), and the
-// member-row ranges they select.
-__global__ void __launch_bounds__(kThreads) top_clusters_kernel(const ClusterLaunch L) {
-  __shared__ float s_v[kWarps];
-  __shared__ int s_i[kWarps];
-  __shared__ int s_sel[SPECDEC_CLUSTER_MAX_TOP_K];
-  grid_launch_dependents();
-  grid_dependency_wait();
-  const int m = blockIdx.x;
+// The top_k largest cluster logits of row m (ties to the lower index) into
+// sel, and the kept members' offsets and first table rows into off
+// [top_k + 1] and row0 (all shared). With `publish`, the kept clusters and
+// offsets also go to global memory for the later kernels, and a kept
+// cluster larger than max_cluster is reported. Every thread of the CTA
+// calls it.
+__device__ __forceinline__ void select_clusters(const ClusterLaunch& L, int m, bool publish,
+                                                int* sel, int* off, int* row0, float* s_v,
+                                                int* s_i) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* y = L.y + (size_t)m * L.n_c;
   for (int k = 0; k < L.top_k; ++k) {
@@ -147,7 +149,7 @@ __global__ void __launch_bounds__(kThreads) top_clusters_kernel(const ClusterLau
     int bi = 0x7fffffff;
     for (int c = threadIdx.x; c < L.n_c; c += kThreads) {
       bool taken = false;
-      for (int j = 0; j < k; ++j) taken |= s_sel[j] == c;
+      for (int j = 0; j < k; ++j) taken |= sel[j] == c;
       const float v = y[c];
       if (!taken && argmax_better(v, c, bv, bi)) {
         bv = v;
@@ -166,32 +168,47 @@ __global__ void __launch_bounds__(kThreads) top_clusters_kernel(const ClusterLau
           bv = s_v[w];
           bi = s_i[w];
         }
-      s_sel[k] = bi;
+      sel[k] = bi;
     }
     __syncthreads();
   }
-  __shared__ int s_off[SPECDEC_CLUSTER_MAX_TOP_K + 1], s_row0[SPECDEC_CLUSTER_MAX_TOP_K];
   if (threadIdx.x == 0) {
-    int off = 0;
+    int o = 0;
     bool bad = false;
     for (int k = 0; k < L.top_k; ++k) {
-      const int c = s_sel[k];
+      const int c = sel[k];
       const int r0 = L.starts[c];
       const int n = L.starts[c + 1] - r0;
       bad |= n < 0 || n > L.max_cluster;
-      L.clusters[(size_t)m * L.top_k + k] = c;
-      L.offs[(size_t)m * (L.top_k + 1) + k] = off;
-      s_off[k] = off;
-      s_row0[k] = r0;
-      off += max(0, min(n, L.max_cluster));
+      off[k] = o;
+      row0[k] = r0;
+      if (publish) {
+        L.clusters[(size_t)m * L.top_k + k] = c;
+        L.offs[(size_t)m * (L.top_k + 1) + k] = o;
+      }
+      o += max(0, min(n, L.max_cluster));
     }
-    L.offs[(size_t)m * (L.top_k + 1) + L.top_k] = off;
-    s_off[L.top_k] = off;
-    if (bad) set_status(L.status, SPECDEC_ERR_INVALID_ARG);
+    off[L.top_k] = o;
+    if (publish) {
+      L.offs[(size_t)m * (L.top_k + 1) + L.top_k] = o;
+      if (bad) set_status(L.status, SPECDEC_ERR_INVALID_ARG);
+    }
   }
   __syncthreads();
-  // The kept members' table rows, in kept order, so the next kernel reads
-  // each member's row with one load (it replaces them by token IDs).
+}
+
+// The kept clusters of row m and their members' table rows, in kept order,
+// so the member kernel reads each row with one load (it replaces them by
+// token IDs).
+__global__ void __launch_bounds__(kThreads) top_clusters_kernel(const ClusterLaunch L) {
+  __shared__ float s_v[kWarps];
+  __shared__ int s_i[kWarps];
+  __shared__ int s_sel[SPECDEC_CLUSTER_MAX_TOP_K];
+  __shared__ int s_off[SPECDEC_CLUSTER_MAX_TOP_K + 1], s_row0[SPECDEC_CLUSTER_MAX_TOP_K];
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int m = blockIdx.x;
+  select_clusters(L, m, true, s_sel, s_off, s_row0, s_v, s_i);
   for (int k = 0; k < L.top_k; ++k)
     for (int i = s_off[k] + threadIdx.x; i < s_off[k + 1]; i += kThreads)
       L.ids[(size_t)m * L.max_members + i] = s_row0[k] + (i - s_off[k]);
@@ -215,6 +232,42 @@ __global__ void __launch_bounds__(kThreads) member_logits_kernel(const ClusterLa
   __syncthreads();
   for (int i = i0 + warp; i < min(total, i0 + kMemberBlock); i += kWarps) {
     const int r = L.ids[(size_t)m * L.max_members + i];   // table row (written by top_clusters)
+    if (r < 0 || r >= L.V) {   // starts outside the table: report, read nothing
+      if (lane == 0) set_status(L.status, SPECDEC_ERR_INVALID_ARG);
+      continue;
+    }
+    const float z = warp_dot(L.W + (size_t)r * L.d, hs, L.d);
+    if (lane == 0) {
+      const int id = L.token_of_row[r];
+      L.z[(size_t)m * L.max_members + i] = z;
+      L.ids[(size_t)m * L.max_members + i] = id;
+      if (L.logits_out != nullptr && id >= 0 && id < L.V) L.logits_out[(size_t)m * L.V + id] = z;
+    }
+  }
+}
+
+// One kept cluster and at most kFuseRows rows: the member kernel selects
+// the cluster itself (every CTA of row m the same way; CTA 0 of the row
+// publishes it), saving the top-k kernel and its launch.
+__global__ void __launch_bounds__(kThreads) member_logits_fused_kernel(const ClusterLaunch L) {
+  __shared__ __align__(16) __nv_bfloat16 hs[SPECDEC_CLUSTER_MAX_D];
+  __shared__ float s_v[kWarps];
+  __shared__ int s_i[kWarps];
+  __shared__ int s_sel[SPECDEC_CLUSTER_MAX_TOP_K];
+  __shared__ int s_off[SPECDEC_CLUSTER_MAX_TOP_K + 1], s_row0[SPECDEC_CLUSTER_MAX_TOP_K];
+  grid_launch_dependents();
+  grid_dependency_wait();
+  const int m = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int e = threadIdx.x; e < L.d / 8; e += kThreads)
+    reinterpret_cast<uint4*>(hs)[e] = __ldg(reinterpret_cast<const uint4*>(L.h + (size_t)m * L.d) + e);
+  select_clusters(L, m, blockIdx.x == 0, s_sel, s_off, s_row0, s_v, s_i);   // ends with a barrier
+  const int total = s_off[L.top_k];
+  const int i0 = blockIdx.x * kMemberBlock;
+  for (int i = i0 + warp; i < min(total, i0 + kMemberBlock); i += kWarps) {
+    int k = 0;
+    while (k + 1 < L.top_k && s_off[k + 1] <= i) ++k;
+    const int r = s_row0[k] + (i - s_off[k]);
     if (r < 0 || r >= L.V) {   // starts outside the table: report, read nothing
       if (lane == 0) set_status(L.status, SPECDEC_ERR_INVALID_ARG);
       continue;
@@ -417,11 +470,15 @@ cudaError_t launch_cluster_head(const ClusterLaunch& L, cudaStream_t stream) {
   e = launch_pdl(logits_fn, dim3((L.n_c + kWarps - 1) / kWarps),
                  dim3(kThreads), smem1, L, stream);
   if (e != cudaSuccess) return e;
-  e = launch_pdl((const void*)top_clusters_kernel, dim3(L.M), dim3(kThreads), 0, L, stream);
-  if (e != cudaSuccess) return e;
-  e = launch_pdl((const void*)member_logits_kernel,
-                 dim3((L.max_members + kMemberBlock - 1) / kMemberBlock, L.M), dim3(kThreads), 0, L,
-                 stream);
+  const dim3 member_grid((L.max_members + kMemberBlock - 1) / kMemberBlock, L.M);
+  if (L.top_k == 1 && L.M <= kFuseRows) {
+    e = launch_pdl((const void*)member_logits_fused_kernel, member_grid, dim3(kThreads), 0, L,
+                   stream);
+  } else {
+    e = launch_pdl((const void*)top_clusters_kernel, dim3(L.M), dim3(kThreads), 0, L, stream);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl((const void*)member_logits_kernel, member_grid, dim3(kThreads), 0, L, stream);
+  }
   if (e != cudaSuccess) return e;
   return launch_pdl((const void*)draw_kernel, dim3(L.M), dim3(kThreads), smem4, L, stream);
 }

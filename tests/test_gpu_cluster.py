@@ -129,3 +129,24 @@ def test_prepared_cluster_head_rereads_hidden():
     got, _ = step(2, 3)
     torch.cuda.synchronize()
     assert np.array_equal(got.cpu().numpy(), want)
+
+
+def test_cluster_head_bad_starts_set_status_one_kept_cluster():
+    """The same report on the path where the member kernel selects the one
+    kept cluster itself (M <= 8, top_k = 1): the last cluster is made the
+    best one for both rows, and its end runs past the table."""
+    import target_model_verify_gb300 as tv
+    x = _head(13, 2, 64, 1000, 8)
+    E = x["E"].clone()
+    E[-1] = (x["h"].float().sum(0) * 4.0).to(torch.bfloat16)
+    starts = x["starts"].clone()
+    starts[-1] = 5000
+    ws = torch.empty(tv._b.specdec_cluster_head_workspace_size(2, 8, 1, 4096), dtype=torch.uint8,
+                     device=DEV)
+    _, cl = tv.cluster_head(x["h"], E, x["W"], starts, x["tor"], top_k=1, max_cluster=4096,
+                            mode=ov.GREEDY, workspace=ws)
+    assert tv.read_status(ws) == tv._b.SPECDEC_ERR_INVALID_ARG
+    assert (cl[:, 0] == 7).all()
+    tv.cluster_head(x["h"], x["E"], x["W"], x["starts"], x["tor"], top_k=1, max_cluster=512,
+                    mode=ov.GREEDY, workspace=ws)
+    assert tv.read_status(ws) == 0

@@ -229,29 +229,56 @@ def _run_oracle_rows(p, q, x, seed, gamma):
     return ov.verify_from_logits(z, zq, x, 1.0, seed, ov.SAMPLE)
 
 
+def _chi_square_chunk(args):
+    """One worker's share: the oracle on `x` under its own seed; returns the
+    first-token counts, the kept count and the bonus-token counts."""
+    p, q, x, seed = args
+    res = _run_oracle_rows(p, q, x, seed=seed, gamma=1)
+    V = p.shape[1]
+    first = np.bincount(res.out_tokens[:, 0], minlength=V)
+    kept = int(np.sum(res.n_accepted == 1))
+    bonus = np.bincount(res.out_tokens[res.n_accepted == 1, 1], minlength=V)
+    return first, kept, bonus
+
+
 @pytest.mark.slow
 def test_chi_square_and_acceptance_rate():
-    """V=64, gamma=1 through the whole oracle (Philox draws included): the
-    first written token follows p0 (chi-square) and the kept fraction matches
-    sum_v min(p0, q0) within 4 binomial sigmas ("推测解码", sections
-    和大模型写的一样 and 接受率 α)."""
+    """10^6 sequences at V=64, gamma=1 through the whole oracle (Philox draws
+    included): the first written token follows p0 (chi-square), the kept
+    fraction matches sum_v min(p0, q0) within 4 binomial sigmas, and bonus
+    tokens after a kept draft follow p1 ("推测解码", sections 和大模型写的一样
+    and 接受率 α). The sequences run as 16 chunks, each under its own seed
+    (independent Philox streams), on a pool of spawned worker processes."""
     scipy_stats = pytest.importorskip("scipy.stats")
+    import concurrent.futures as cf
+    import multiprocessing as mp
     rng = np.random.default_rng(77)
-    V, B = 64, 100_000
+    V, B, chunks = 64, 1_000_000, 16
     p = rng.dirichlet(np.ones(V), size=2)
     q = rng.dirichlet(np.ones(V) * 0.5, size=1)
     x = rng.choice(V, size=(B, 1), p=q[0])
-    res = _run_oracle_rows(p, q, x, seed=31337, gamma=1)
-    first = res.out_tokens[:, 0]
-    counts = np.bincount(first, minlength=V)
+    parts = [(p, q, x[c * (B // chunks):(c + 1) * (B // chunks)], 31337 + c) for c in range(chunks)]
+    workers = max(1, min(chunks, len(os.sched_getaffinity(0))))
+    env = {k: os.environ.get(k) for k in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS")}
+    for k in env:
+        os.environ[k] = "1"   # one BLAS thread per worker (inherited by the spawned processes)
+    try:
+        with cf.ProcessPoolExecutor(max_workers=workers, mp_context=mp.get_context("spawn")) as ex:
+            outs = list(ex.map(_chi_square_chunk, parts))
+    finally:
+        for k, v in env.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v
+    counts = sum(o[0] for o in outs)
+    kept = sum(o[1] for o in outs)
+    c1 = sum(o[2] for o in outs)
+    assert counts.sum() == B
     stat = scipy_stats.chisquare(counts, p[0] * B)
     assert stat.pvalue > 1e-4, stat
     alpha = np.minimum(p[0], q[0]).sum()
-    kept = np.mean(res.n_accepted == 1)
-    assert abs(kept - alpha) < 4 * math.sqrt(alpha * (1 - alpha) / B)
-    # bonus tokens (after a kept draft) follow p1
-    bonus = res.out_tokens[res.n_accepted == 1, 1]
-    c1 = np.bincount(bonus, minlength=V)
+    assert abs(kept / B - alpha) < 4 * math.sqrt(alpha * (1 - alpha) / B)
     assert scipy_stats.chisquare(c1, p[1] * c1.sum()).pvalue > 1e-4
 
 

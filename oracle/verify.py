@@ -92,6 +92,19 @@ def accept_test(p_x, q_x, r):
     return np.asarray(r) * np.asarray(q_x) <= np.asarray(p_x)
 
 
+def accept_margin(p_x: float, q_x: float, r: float) -> float:
+    """Distance of the acceptance uniform r from the threshold p(x)/q(x).
+
+    The keep/reject decision of "推测解码", section 通过的规则, flips only if
+    r moves across p/q, so |r - p/q| is how far that decision is from being
+    taken the other way. A draft whose q underflowed to 0 is kept for every
+    r (the limit of min(1, p/q)), so its margin is infinite.
+    """
+    if not q_x > 0:
+        return float("inf")
+    return abs(r - p_x / q_x)
+
+
 def residual_weights(p_row, q_row) -> np.ndarray:
     """w = max(0, p - q), the part of p that q under-covers.
 
@@ -160,7 +173,7 @@ def verify_sequence_sampling(p_rows, q_rows, x, r, u_at) -> SequenceResult:
     for i in range(gamma):
         p_x = p_rows[i, x[i]]
         q_x = q_rows[i, x[i]]
-        res.accept_margins.append(abs(r[i] - p_x / q_x) if q_x > 0 else float("inf"))
+        res.accept_margins.append(accept_margin(p_x, q_x, r[i]))
         if accept_test(p_x, q_x, r[i]):
             tokens[i] = x[i]
         else:

@@ -218,6 +218,84 @@ def test_invert_cdf_boundaries():
     assert abs(m - 0.05) < 1e-15
 
 
+# ------------------------------------------------ decision margins --
+# The parity rule forgives a token mismatch only where the oracle's decision
+# was close: |r - p/q| < 1e-4 for an acceptance test, u within 1e-4 of a CDF
+# boundary for a draw, a top-2 logit gap below 1e-3 in greedy mode. A wrong
+# margin would silently widen what the rule forgives, so each is pinned to
+# values worked out by hand below.
+
+def check_accept_margins():
+    """The page's worked fragment ("推测解码", section 和大模型写的一样):
+    p = (0.32, 0.09, 0.59), q = (0.13, 0.33, 0.54) over (地, 慢, third).
+    Drafts x = (慢, 地) with r = (0.2, 0.5): p/q(慢) = 0.09/0.33 = 3/11, so
+    r = 0.2 keeps it with margin 3/11 - 1/5 = 4/55; p/q(地) = 0.32/0.13 =
+    32/13 (> 1), so r = 0.5 keeps it with margin 32/13 - 1/2 = 51/26. With
+    r = (0.5, .) the first test fails with margin 1/2 - 3/11 = 5/22 and no
+    second test is taken. A draft with q(x) = 0 is kept at any r: margin inf."""
+    p = np.array([0.32, 0.09, 0.59])
+    q = np.array([0.13, 0.33, 0.54])
+    rows_p = np.stack([p, p, p])
+    rows_q = np.stack([q, q])
+    u_at = lambda j: 0.5
+    s = ov.verify_sequence_sampling(rows_p, rows_q, np.array([1, 0]), np.array([0.2, 0.5]), u_at)
+    assert s.n_accepted == 2
+    assert len(s.accept_margins) == 2
+    assert abs(s.accept_margins[0] - 4.0 / 55.0) < 1e-15, s.accept_margins
+    assert abs(s.accept_margins[1] - 51.0 / 26.0) < 1e-14, s.accept_margins
+    s = ov.verify_sequence_sampling(rows_p, rows_q, np.array([1, 0]), np.array([0.5, 0.5]), u_at)
+    assert s.n_accepted == 0 and len(s.accept_margins) == 1
+    assert abs(s.accept_margins[0] - 5.0 / 22.0) < 1e-15, s.accept_margins
+    pz = np.array([[0.5, 0.5, 0.0], [0.5, 0.5, 0.0]])
+    qz = np.array([[0.0, 1.0, 0.0]])
+    s = ov.verify_sequence_sampling(pz, qz, np.array([0]), np.array([1.0]), u_at)
+    assert s.n_accepted == 1 and s.accept_margins == [math.inf]
+
+
+def check_greedy_gaps():
+    """Top-1 minus top-2 logit, by hand: (0.1, 0.7, 0.4, -1) -> token 1,
+    gap 0.7 - 0.4 = 0.3; an exact tie (1, 3, 2.5, 3) -> the lower ID 1 and
+    gap 0; three equal maxima -> token 0, gap 0; one token -> gap inf. In a
+    sequence, the gaps of every row the walk tested are kept in order."""
+    v, gap = ov.greedy_argmax([0.1, 0.7, 0.4, -1.0])
+    assert v == 1 and abs(gap - 0.3) < 1e-15
+    assert ov.greedy_argmax([1.0, 3.0, 2.5, 3.0]) == (1, 0.0)
+    assert ov.greedy_argmax([2.0, 2.0, 2.0]) == (0, 0.0)
+    assert ov.greedy_argmax([5.0]) == (0, math.inf)
+    z = np.array([[0.0, 2.0, 1.5], [4.0, 1.0, 3.0], [0.0, 0.0, 9.0]])
+    s = ov.verify_sequence_greedy(z, np.array([1, 2]))
+    assert s.n_accepted == 1 and list(s.tokens) == [1, 0, -1]
+    np.testing.assert_allclose(s.greedy_gaps, [0.5, 1.0], rtol=0, atol=1e-15)
+
+
+def check_draw_margins():
+    """w = (1, 2, 1): C = (1, 3, 4), S = 4, token 1 owns [1/4, 3/4) of u.
+    u = 0.3 sits 0.05 above its lower edge and u = 0.7 0.05 below its upper
+    edge (margin 0.05 both times); u = 0.74 is 0.01 from the upper edge;
+    u = 0.25 and u = 0.75 sit exactly on a boundary (margin 0, tokens 1 and
+    2 under the strict C_v > u S); u = 0.9 is token 2, 0.1 from its upper
+    edge; u = 0 is token 0 on its lower edge."""
+    w = np.array([1.0, 2.0, 1.0])
+    cases = [(0.3, 1, 0.05), (0.7, 1, 0.05), (0.74, 1, 0.01), (0.25, 1, 0.0), (0.75, 2, 0.0),
+             (0.9, 2, 0.1), (0.0, 0, 0.0)]
+    for u, tok, margin in cases:
+        v, m = ov.invert_cdf(w, u)
+        assert int(v) == tok, (u, v)
+        assert abs(float(m) - margin) < 1e-15, (u, m, margin)
+
+
+def test_accept_margin_pin():
+    check_accept_margins()
+
+
+def test_greedy_gap_pin():
+    check_greedy_gaps()
+
+
+def test_draw_margin_pin():
+    check_draw_margins()
+
+
 # ------------------------------------------------------------- statistics --
 
 def _run_oracle_rows(p, q, x, seed, gamma):
@@ -423,3 +501,72 @@ def test_pins_catch_a_weak_inequality_in_the_draw(monkeypatch):
     monkeypatch.setattr(ov, "invert_cdf", bad_invert)
     res = _draw_law(np.array([0.0, 0.5, 0.5]), 3)
     assert res[0] > 0
+
+
+def test_pins_catch_an_inverted_accept_margin(monkeypatch):
+    """A margin measured against q/p instead of p/q fails its pin."""
+    monkeypatch.setattr(ov, "accept_margin",
+                        lambda px, qx, r: abs(r - qx / px) if px > 0 else math.inf)
+    with pytest.raises(AssertionError):
+        check_accept_margins()
+
+
+def test_pins_catch_a_margin_from_one(monkeypatch):
+    """A margin taken as the distance of p/q from 1 (ignoring r) fails."""
+    monkeypatch.setattr(ov, "accept_margin",
+                        lambda px, qx, r: abs(1.0 - px / qx) if qx > 0 else math.inf)
+    with pytest.raises(AssertionError):
+        check_accept_margins()
+
+
+def test_pins_catch_a_top1_minus_top3_gap(monkeypatch):
+    """A gap to the third-largest logit instead of the second fails."""
+    def bad(z_row):
+        z_row = np.asarray(z_row, dtype=np.float64)
+        v = int(np.argmax(z_row))
+        if z_row.shape[0] < 3:
+            return v, math.inf
+        top3 = np.sort(z_row)[-3:]
+        return v, float(top3[2] - top3[0])
+    monkeypatch.setattr(ov, "greedy_argmax", bad)
+    with pytest.raises(AssertionError):
+        check_greedy_gaps()
+
+
+def test_pins_catch_a_gap_that_skips_ties(monkeypatch):
+    """A gap to the next distinct value (so an exact tie reads as a wide
+    margin) fails."""
+    def bad(z_row):
+        z_row = np.asarray(z_row, dtype=np.float64)
+        v = int(np.argmax(z_row))
+        vals = np.unique(z_row)
+        return v, float(vals[-1] - vals[-2]) if vals.shape[0] > 1 else math.inf
+    monkeypatch.setattr(ov, "greedy_argmax", bad)
+    with pytest.raises(AssertionError):
+        check_greedy_gaps()
+
+
+def test_pins_catch_a_lower_edge_only_draw_margin(monkeypatch):
+    """A draw margin measured to the lower edge only fails at u = 0.7."""
+    good = ov.invert_cdf
+
+    def bad(w, u):
+        C = np.cumsum(np.asarray(w, dtype=np.float64))
+        v, _ = good(w, u)
+        lo = C[v - 1] if v > 0 else 0.0
+        return v, (np.asarray(u) * C[-1] - lo) / C[-1]
+    monkeypatch.setattr(ov, "invert_cdf", bad)
+    with pytest.raises(AssertionError):
+        check_draw_margins()
+
+
+def test_pins_catch_an_unnormalised_draw_margin(monkeypatch):
+    """A draw margin left in units of w (not divided by S) fails."""
+    good = ov.invert_cdf
+
+    def bad(w, u):
+        v, m = good(w, u)
+        return v, m * np.cumsum(np.asarray(w, dtype=np.float64))[-1]
+    monkeypatch.setattr(ov, "invert_cdf", bad)
+    with pytest.raises(AssertionError):
+        check_draw_margins()

@@ -37,10 +37,17 @@ struct PartialQ {
   float m;
   float s;
 };
-// What the sampler needs about the row each sequence samples from.
+// What the sampler needs about the row each sequence samples from. The
+// draw only needs the weights up to one common factor, so with
+// e_p(v) = exp2((z_v - mp) c) and e_q(v) = exp2((zq_v - mq) c) it uses
+// w(v) = e_p(v) (bonus) or max(0, e_p(v) - R e_q(v)) (residual), where
+// R = s_p / s_q is the ratio of the two rows' exp2 sums, held as an
+// unevaluated fp32 pair r_hi + r_lo so that the balance of p against q
+// keeps fp64 accuracy.
 struct SelectedRow {
-  float mp, lsp;      // max z and log2 of its sum, row j of the target
-  float mq, lsq;      // the same for the draft row j (residual case)
+  float mp;           // max z of target row j
+  float mq;           // max draft logit of draft row j (residual case)
+  float r_hi, r_lo;   // R = r_hi + r_lo (residual case)
   int residual;       // 1: w = max(0, p - q); 0: w = p (bonus)
   int j;              // the position sampled (n_accepted), or -1: nothing to draw
   int pad[2];
@@ -122,6 +129,11 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 __device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+  return x;
+}
+__device__ __forceinline__ double warp_sum_d(double x) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;

@@ -14,6 +14,16 @@
 // sequence to finish (atomic ticket, no waiting) forms the prefix of the
 // chunk sums with one warp, finds the chunk holding t, rescans that chunk in
 // token order (16 contiguous tokens per thread) and writes the token.
+//
+// Precision: with ~10^5 tokens each token's interval is ~1e-5 of the unit
+// range, and any error in the boundaries C_v / S changes the drawn token
+// for that share of the uniforms. So the weights are taken up to a common
+// factor (no fp32 normaliser: bonus w = e_p, residual w = max(0, e_p -
+// R e_q) with the p/q balance R as an fp32 pair applied by two fused
+// multiply-adds), each thread's 16 weights are summed in fp32 and everything
+// above that -- chunk sums, their prefix, the target t and each thread's
+// offset -- in fp64. The rescan compares each thread's own fp32 running sum
+// with t minus the thread's fp64 offset.
 #include "kernels.h"
 
 namespace specdec {
@@ -63,29 +73,32 @@ __device__ __forceinline__ Raw4 load4(const float* __restrict__ zr, const DL* __
   return r;
 }
 
-// w = max(0, p - q) (residual) or p, for the four tokens of a group.
+// w = max(0, e_p - R e_q) (residual) or e_p (bonus), for the four tokens
+// of a group, e_p = exp2((z - mp) c), e_q = exp2((zq - mq) c).
 __device__ __forceinline__ void weights4(const Raw4& r, const SelectedRow& sr, bool residual,
                                          float c, float* w) {
   const float zz[kVec] = {r.z.x, r.z.y, r.z.z, r.z.w};
 #pragma unroll
   for (int e = 0; e < kVec; ++e) {
-    const float p = exp2f((zz[e] - sr.mp) * c - sr.lsp);
+    const float ep = exp2f((zz[e] - sr.mp) * c);
     if (residual) {
-      const float qv = exp2f((r.q[e] - sr.mq) * c - sr.lsq);
-      w[e] = fmaxf(0.f, p - qv);
+      const float eq = exp2f((r.q[e] - sr.mq) * c);
+      // R e_q - e_p with R = r_hi + r_lo: one rounding for the main term.
+      const float d = fmaf(eq, sr.r_lo, fmaf(eq, sr.r_hi, -ep));
+      w[e] = fmaxf(0.f, -d);
     } else {
-      w[e] = p;
+      w[e] = ep;
     }
   }
 }
 
-// Sum of one chunk's weights: four coalesced sweeps, thread-sequential,
-// then warp shuffles, then the 8 warp sums in order. Every thread returns
-// the chunk total.
+// Sum of one chunk's weights: four coalesced sweeps, thread-sequential in
+// fp32, then warp shuffles and the 8 warp sums in order, in fp64. Every
+// thread returns the chunk total.
 template <typename DL>
-__device__ __forceinline__ float chunk_total(const float* zr, const DL* qr, const SelectedRow& sr,
-                                             bool residual, float c, int V, bool vec, int chunk,
-                                             float* red) {
+__device__ __forceinline__ double chunk_total(const float* zr, const DL* qr, const SelectedRow& sr,
+                                              bool residual, float c, int V, bool vec, int chunk,
+                                              double* red) {
   const int v0 = chunk * kChunkV + threadIdx.x * kVec;
   Raw4 raw[kSweeps];
 #pragma unroll
@@ -98,33 +111,33 @@ __device__ __forceinline__ float chunk_total(const float* zr, const DL* qr, cons
 #pragma unroll
     for (int e = 0; e < kVec; ++e) ts += w[e];
   }
-  ts = warp_sum(ts);
+  const double tsd = warp_sum_d((double)ts);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
-  if (lane == 0) red[warp] = ts;
+  if (lane == 0) red[warp] = tsd;
   __syncthreads();
-  float t = 0.f;
+  double t = 0.0;
   for (int i = 0; i < kSampleThreads / 32; ++i) t += red[i];
   return t;
 }
 
 // Warp 0: inclusive prefix of the chunk sums in chunk order (groups of 32,
-// shuffle scan, carried total), and the last chunk holding weight.
-__device__ __forceinline__ void prefix_chunks(const float* cs, float* pre, int n, int* last_pos) {
+// fp64 shuffle scan, carried total), and the last chunk holding weight.
+__device__ __forceinline__ void prefix_chunks(const double* cs, double* pre, int n, int* last_pos) {
   const int lane = threadIdx.x & 31;
-  float carry = 0.f;
+  double carry = 0.0;
   int lp = -1;
   for (int g = 0; g < n; g += 32) {
     const int k = g + lane;
-    const float x = k < n ? cs[k] : 0.f;
-    float incl = x;
+    const double x = k < n ? cs[k] : 0.0;
+    double incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, incl, o);
+      const double y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
     if (k < n) pre[k] = carry + incl;
-    const unsigned pos = __ballot_sync(0xffffffffu, k < n && x > 0.f);
+    const unsigned pos = __ballot_sync(0xffffffffu, k < n && x > 0.0);
     if (pos) lp = g + 31 - __clz(pos);
     carry += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -133,16 +146,16 @@ __device__ __forceinline__ void prefix_chunks(const float* cs, float* pre, int n
 
 template <typename DL>
 __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaunch L) {
-  __shared__ float red[kSampleThreads / 32];
-  __shared__ float wscan[kSampleThreads / 32];
-  __shared__ float s_cs[kMaxChunks];
-  __shared__ float s_pre[kMaxChunks];
+  __shared__ double red[kSampleThreads / 32];
+  __shared__ double wscan[kSampleThreads / 32];
+  __shared__ double s_cs[kMaxChunks];
+  __shared__ double s_pre[kMaxChunks];
   __shared__ int s_last;
   __shared__ int s_tok;
   __shared__ int s_lastpos;
   __shared__ int s_lastchunk;
   __shared__ int s_chunk;
-  __shared__ float s_before, s_t;
+  __shared__ double s_before, s_t;
   __shared__ int s_residual;
 
   const int b = blockIdx.y;
@@ -173,7 +186,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
-  const float total = chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, vec, chunk, red);
+  const double total = chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, vec, chunk, red);
   if (tid == 0) {
     L.chunk_sums[(size_t)b * L.nchunks + chunk] = total;
     __threadfence();
@@ -185,18 +198,18 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   __threadfence();
 
   // ---- last CTA of sequence b: locate the chunk holding t = u * S ----
-  const float u = sample_uniform(L.seed, b, sr.j);
+  const double u = (double)sample_uniform(L.seed, b, sr.j);
   for (int k = tid; k < L.nchunks; k += kSampleThreads)
     s_cs[k] = __ldcg(L.chunk_sums + (size_t)b * L.nchunks + k);
   __syncthreads();
   if (warp == 0) prefix_chunks(s_cs, s_pre, L.nchunks, &s_lastchunk);
   __syncthreads();
   bool residual = sr.residual != 0;
-  if (residual && !(s_pre[L.nchunks - 1] > 0.f)) {
+  if (residual && !(s_pre[L.nchunks - 1] > 0.0)) {
     // p == q to rounding: draw from p. Recompute every chunk sum with w = p.
     residual = false;
     for (int k = 0; k < L.nchunks; ++k) {
-      const float tot = chunk_total<DL>(zr, qr, sr, false, L.c, L.V, vec, k, red);
+      const double tot = chunk_total<DL>(zr, qr, sr, false, L.c, L.V, vec, k, red);
       if (tid == 0) s_cs[k] = tot;
     }
     __syncthreads();
@@ -204,7 +217,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
     __syncthreads();
   }
   if (warp == 0) {
-    const float t = u * s_pre[L.nchunks - 1];
+    const double t = u * s_pre[L.nchunks - 1];
     int found = -1;
     for (int g = 0; g < L.nchunks && found < 0; g += 32) {
       const int k = g + lane;
@@ -215,7 +228,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
     if (found < 0) found = 0;             // no weight at all (cannot happen for w = p)
     if (lane == 0) {
       s_chunk = found;
-      s_before = found > 0 ? s_pre[found - 1] : 0.f;
+      s_before = found > 0 ? s_pre[found - 1] : 0.0;
       s_t = t;
       s_tok = 0x7fffffff;
       s_lastpos = -1;
@@ -235,26 +248,27 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   float ts = 0.f;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) ts += w[k];
-  float incl = ts;
+  double incl = (double)ts;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    const double y = __shfl_up_sync(0xffffffffu, incl, o);
     if (lane >= o) incl += y;
   }
-  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) excl = 0.f;
+  double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.0;
   if (lane == 31) wscan[warp] = incl;
   __syncthreads();
-  float wbefore = 0.f;
+  double wbefore = 0.0;
   for (int i = 0; i < warp; ++i) wbefore += wscan[i];
-  float run = s_before + (wbefore + excl);
-  const float t = s_t;
+  // This thread's tokens against t measured from the thread's first token.
+  const float t_loc = (float)(s_t - (s_before + (wbefore + excl)));
+  float run = 0.f;
   int cand = 0x7fffffff, lastp = -1;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     run += w[k];
     if (w[k] > 0.f) lastp = v0 + k;
-    if (cand == 0x7fffffff && w[k] > 0.f && run > t) cand = v0 + k;
+    if (cand == 0x7fffffff && w[k] > 0.f && run > t_loc) cand = v0 + k;
   }
   if (cand != 0x7fffffff) atomicMin(&s_tok, cand);
   if (lastp >= 0) atomicMax(&s_lastpos, lastp);

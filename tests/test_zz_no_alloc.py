@@ -70,3 +70,46 @@ def test_noalloc_matches_workspace_entry_point(name, mode):
         np.testing.assert_array_equal(out.cpu().numpy(), ref_out.cpu().numpy())
         np.testing.assert_array_equal(nacc.cpu().numpy(), ref_nacc.cpu().numpy())
         assert 0 <= int(nacc[0]) <= w.gamma
+
+
+@pytest.mark.gpu
+def test_noalloc_leftovers_of_other_shapes_and_a_failed_call_do_no_harm():
+    """The shared array keeps whatever the previous call left: its header,
+    fix-up tickets and sampler counters laid out for another shape or mode,
+    or the state of a call that failed on the device. A sequence of calls
+    of different shapes and modes, with one failed call in the middle (a
+    draft token outside [0, V): that sequence reports n_accepted = -1 and
+    -1 tokens), must give every valid call exactly the workspace entry
+    point's tokens."""
+    import target_model_verify_gb300 as tv
+    from target_model_verify_gb300 import build
+    build.build()
+    llama = wl.get("llama3_8b_head", B=2)
+    tiny = wl.get("tiny_fp32")
+    x_llama = wl.generate(llama, 41, device="cuda:0")
+    x_tiny = wl.generate(tiny, 42, device="cuda:0")
+    bad = dict(x_llama, draft_tokens=x_llama["draft_tokens"].clone())
+    bad["draft_tokens"][1, 2] = llama.V
+
+    def check(w, inp, mode, seed):
+        dl = inp["draft_logits"] if mode == b.SPECDEC_SAMPLE else None
+        ref_out, ref_nacc = tv.verify(inp["hidden"], inp["W_lm"], inp["draft_tokens"], dl,
+                                      w.temperature, seed, mode)
+        out = torch.full_like(ref_out, -7)
+        nacc = torch.full_like(ref_nacc, -7)
+        assert _noalloc(inp, w.temperature, seed, mode, out, nacc, dl) == b.SPECDEC_OK
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(out.cpu().numpy(), ref_out.cpu().numpy())
+        np.testing.assert_array_equal(nacc.cpu().numpy(), ref_nacc.cpu().numpy())
+
+    check(llama, x_llama, b.SPECDEC_SAMPLE, 5)
+    check(tiny, x_tiny, b.SPECDEC_SAMPLE, 6)
+    check(llama, x_llama, b.SPECDEC_GREEDY, 7)
+    out = torch.full((llama.B, llama.gamma + 1), -7, dtype=torch.int32, device="cuda:0")
+    nacc = torch.full((llama.B,), -7, dtype=torch.int32, device="cuda:0")
+    assert _noalloc(bad, 1.0, 8, b.SPECDEC_SAMPLE, out, nacc, bad["draft_logits"]) == b.SPECDEC_OK
+    torch.cuda.synchronize()
+    assert int(nacc[1]) == -1 and bool((out[1] == -1).all())
+    assert 0 <= int(nacc[0]) <= llama.gamma
+    check(llama, x_llama, b.SPECDEC_SAMPLE, 9)
+    check(tiny, x_tiny, b.SPECDEC_SAMPLE, 10)

@@ -44,6 +44,7 @@ LMHEAD_SOURCES = ["target_model_verify_gb300/csrc/lmhead_tc.cu",
                   "target_model_verify_gb300/csrc/common.cuh"]
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CPU_BASELINE_SECONDS = 10.0
+CLOCK_WINDOW_SECONDS = 1.5
 REFERENCE_BUDGET_SECONDS = 150.0
 
 
@@ -142,7 +143,7 @@ class ClockSampler:
             out, _ = self.proc.communicate()
         self.lines = [ln for ln in out.splitlines() if ln.strip()]
 
-    def summary(self, t0: float, t1: float):
+    def summary(self, t0: float, t1: float, strict: bool = False):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
         rows = []
@@ -155,7 +156,10 @@ class ClockSampler:
                 rows.append((ts, float(parts[1]), float(parts[2]), parts[5:9]))
             except ValueError:
                 continue
-        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05] or rows
+        inside = [r for r in rows if t0 - 0.05 <= r[0] <= t1 + 0.05]
+        if strict and not inside:
+            return {"samples": 0}
+        inside = inside or rows
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -170,6 +174,65 @@ def host_cores() -> int:
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def _openblas_fns():
+    """get/set functions of the OpenBLAS that NumPy loaded, or (None, None)."""
+    import ctypes
+    try:
+        with open("/proc/self/maps") as f:
+            paths = sorted({ln.split()[-1] for ln in f if "openblas" in ln.lower() and ".so" in ln})
+    except OSError:
+        return None, None
+    for path in paths:
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for pre in ("scipy_openblas_", "openblas_", ""):
+            for suf in ("64_", ""):
+                g = getattr(lib, f"{pre}get_num_threads{suf}", None) if pre else None
+                st = getattr(lib, f"{pre}set_num_threads{suf}", None) if pre else None
+                if g is not None and st is not None:
+                    g.restype = ctypes.c_int
+                    st.argtypes = [ctypes.c_int]
+                    return g, st
+    return None, None
+
+
+def blas_threads():
+    """Threads NumPy's BLAS uses (None if it cannot be asked)."""
+    get, _ = _openblas_fns()
+    return int(get()) if get is not None else None
+
+
+def time_oracle_one_thread(w, inp, mode, budget_s: float):
+    """time_oracle with NumPy's BLAS limited to one thread (restored after)."""
+    get, set_ = _openblas_fns()
+    if get is None:
+        return None
+    n0 = int(get())
+    set_(1)
+    try:
+        return time_oracle(w, inp, mode, budget_s)
+    finally:
+        set_(n0)
+
+
+def bench_config(args, w, world) -> dict:
+    """The `config` object, identical in both arms for the same workload."""
+    return {"workload": args.workload, "B": w.B, "gamma": w.gamma, "d": w.d, "V": w.V,
+            "mode": args.mode, "temperature": w.temperature,
+            **({"tree_nodes": w.N, "tree_depth": tree_depth(w.tree)}
+               if w.tree is not None else {}),
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (W_lm exceeds the 129 MB L2), no flush"}
+
+
+# Workloads whose CPU baseline also reports the oracle on one thread: the
+# small case and the single-sequence heads.
+ONE_THREAD_WORKLOADS = ("tiny_fp32", "llama3_8b_head") + tuple(
+    f"gemma_e2b_head_g{g}" for g in (1, 2, 3, 4, 6, 8))
 
 
 def oracle_inputs(inp: dict, mode: int):
@@ -276,6 +339,17 @@ def run_ours(args, world, rank, local):
     for i in range(Wm):
         step(i)
     torch.cuda.synchronize()
+    # Clock window: the same steps, untimed, for CLOCK_WINDOW_SECONDS right
+    # before the timed region, so that the clock record holds enough
+    # nvidia-smi samples (one per 100 ms) of this load even when the timed
+    # region itself lasts a few milliseconds.
+    t_clock0 = time.time()
+    settle = 0
+    while time.time() - t_clock0 < CLOCK_WINDOW_SECONDS:
+        for _ in range(10):
+            step(Wm - 1)
+        settle += 10
+        torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -351,10 +425,20 @@ def run_ours(args, world, rank, local):
     if world == 1 and not args.no_cpu_baseline:
         v, n = time_oracle(w, inp, mode, CPU_BASELINE_SECONDS)
         cpu = {"value": v, "unit": "steps/s", "cores": host_cores(), "kind": "oracle",
+               "blas_threads": blas_threads(),
                "sample": f"{n} full {args.workload} steps (fp64 NumPy oracle, W converted "
                          f"to fp64 once outside the timing)"}
+        if args.workload in ONE_THREAD_WORKLOADS:
+            one = time_oracle_one_thread(w, inp, mode, CPU_BASELINE_SECONDS)
+            if one is not None:
+                cpu["one_thread"] = {"value": one[0], "unit": "steps/s", "steps": one[1]}
 
-    clocks = sampler.summary(t_wall0, t_wall1) if sampler else None
+    clocks = None
+    if sampler:
+        clocks = sampler.summary(t_clock0, t_wall1)
+        clocks["timed_region_samples"] = sampler.summary(t_wall0, t_wall1, strict=True).get("samples", 0)
+        clocks["window"] = (f"{CLOCK_WINDOW_SECONDS:.1f} s of the same steps ({settle}, untimed) "
+                            f"just before the timed region, and the timed region")
     line = {
         "metric": METRIC,
         "value": steps_per_s,
@@ -368,12 +452,7 @@ def run_ours(args, world, rank, local):
         "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32",
         "data": "synthetic (seeded; random-init LM head)",
-        "config": {"workload": args.workload, "B": w.B, "gamma": w.gamma, "d": w.d, "V": w.V,
-                   "mode": args.mode, "temperature": w.temperature,
-                   **({"tree_nodes": w.N, "tree_depth": tree_depth(w.tree)}
-                      if w.tree is not None else {}),
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (W_lm exceeds the 129 MB L2), no flush"},
+        "config": bench_config(args, w, world),
         "committed_tokens_per_s": steps_per_s * tokens_per_step,
         "mean_tokens_per_step": tokens_per_step,
         "step_roofline": {"time_us": max(t_hbm, t_tc) * 1e6, "frac": max(t_hbm, t_tc) / step_s,
@@ -500,18 +579,17 @@ def run_reference(args, world, rank, local):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 / value,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64", "data": "synthetic (seeded; random-init LM head)",
-        "config": {"workload": args.workload, "B": w.B, "gamma": w.gamma, "d": w.d, "V": w.V,
-                   "mode": args.mode, "temperature": w.temperature},
+        "config": bench_config(args, w, world),
         "impl": "reference",
         "cpu_baseline": {"value": value, "unit": "steps/s", "cores": host_cores(),
-                         "kind": "oracle", "sample": sample},
+                         "blas_threads": blas_threads(), "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "steps/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
 
 
-def run_loop(args):
+def loop_measure(workload: str, c: float, K: int, Wm: int, seed: int = 0) -> dict:
     """The draft -> verify loop on one GPU, against its closed form.
 
     "推测解码", section 快多少: with acceptance rate alpha, gamma guesses per
@@ -522,25 +600,29 @@ def run_loop(args):
     = sum_v min(p, q); the drafter is a GPU busy-wait of c target steps per
     guess, its guesses fresh draws from q every step; the target step is the
     LM head scoring one position (a greedy verify of one guess reads W once).
+
+    Besides the page's closed form, the verify step's own cost is charged in
+    a second one: the verify step timed alone (gamma + 1 positions, the
+    acceptance scan and the draw) in units of the target step replaces the
+    1 in gamma*c + 1.
     """
     import target_model_verify_gb300 as tv
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    w = wl.get(args.workload)
+    w = wl.get(workload)
     if w.tree is not None:
-        raise SystemExit("--loop-c runs the chain step")
+        raise SystemExit("the loop timer runs the chain step")
     B, gamma, d, V, T = w.B, w.gamma, w.d, w.V, w.temperature
-    base = wl.generate(w, args.seed, device=device)
+    base = wl.generate(w, seed, device=device)
     W = base["W_lm"]
     hidden = base["hidden"][:, :1].expand(B, gamma + 1, d).contiguous()
     dl = base["draft_logits"][:, :1].expand(B, gamma, V).contiguous()
-    p = torch.softmax((hidden[:, 0].float() @ W.float().T) / T, dim=-1)
-    q = torch.softmax(dl[:, 0].float() / T, dim=-1)
+    p = torch.softmax((hidden[:, 0].double() @ W.double().T) / T, dim=-1)
+    q = torch.softmax(dl[:, 0].double() / T, dim=-1)
     alpha = float(torch.minimum(p, q).sum(dim=-1).mean())
-    K, Wm = args.steps, args.warmup
     g = torch.Generator(device=device)
-    g.manual_seed(args.seed + 17)
-    draws = torch.multinomial(q, (K + Wm) * gamma, replacement=True, generator=g)
+    g.manual_seed(seed + 17)
+    draws = torch.multinomial(q.float(), (K + Wm) * gamma, replacement=True, generator=g)
     drafts = draws.view(B, K + Wm, gamma).transpose(0, 1).contiguous().int()
     ws = tv.alloc_workspace(B, gamma, d, V, W.dtype, wl.SAMPLE, device=device)
     out = torch.empty(B, gamma + 1, dtype=torch.int32, device=device)
@@ -563,16 +645,19 @@ def run_loop(args):
     ws1 = tv.alloc_workspace(B, 1, d, V, W.dtype, wl.GREEDY, device=device)
     t_target = timed(lambda i: tv.verify(h1, W, drafts[0][:, :1].contiguous(), None, T, i,
                                          wl.GREEDY, workspace=ws1), 300)
+    # the verify step alone, on the loop's own inputs
+    t_verify = timed(lambda i: tv.verify(hidden, W, drafts[i % (K + Wm)], dl, T, i, wl.SAMPLE,
+                                         out_tokens=out, n_accepted=naccs[0], workspace=ws), 300)
     # the drafter: a busy-wait calibrated in SM cycles
     calib = 2_000_000
     us_per_cycle = timed(lambda i: torch.cuda._sleep(calib), 20) / calib
-    draft_cycles = max(1, int(args.loop_c * t_target / us_per_cycle))
+    draft_cycles = max(1, int(c * t_target / us_per_cycle))
     t_draft = timed(lambda i: torch.cuda._sleep(draft_cycles), 200)
 
     def step(i):
         for _ in range(gamma):
             torch.cuda._sleep(draft_cycles)
-        tv.verify(hidden, W, drafts[i], dl, T, args.seed * 1_000_003 + i, wl.SAMPLE,
+        tv.verify(hidden, W, drafts[i], dl, T, seed * 1_000_003 + i, wl.SAMPLE,
                   out_tokens=out, n_accepted=naccs[i], workspace=ws)
 
     for i in range(Wm):
@@ -585,22 +670,33 @@ def run_loop(args):
     e1.record()
     torch.cuda.synchronize()
     t_step = e0.elapsed_time(e1) * 1e3 / K
-    tokens = float((naccs[Wm:].double() + 1).mean())
+    n = (naccs[Wm:].double() + 1).flatten()
+    tokens = float(n.mean())
     c_eff = t_draft / t_target
     tok_closed = (1 - alpha ** (gamma + 1)) / (1 - alpha)
-    line = {
+    pk = [alpha ** k * (1 - alpha) for k in range(gamma)] + [alpha ** gamma]
+    var = sum(pk[k] * (k + 1) ** 2 for k in range(gamma + 1)) - tok_closed ** 2
+    sigma = (tokens - tok_closed) / math.sqrt(var / n.numel())
+    return {
         "metric": "speculative decoding speed-up over one token per target step (draft->verify loop)",
         "value": tokens * t_target / t_step,
         "unit": "x",
         "closed_form": tok_closed / (gamma * c_eff + 1),
-        "closed_form_with_verify_cost": tok_closed / (gamma * c_eff + (t_step - gamma * t_draft) / t_target),
+        "closed_form_with_verify_cost": tok_closed / (gamma * c_eff + t_verify / t_target),
+        "speedup_at_closed_form_tokens": tok_closed * t_target / t_step,
+        "tokens_per_step_law_sigma": sigma,
         "alpha": alpha, "gamma": gamma, "c": c_eff, "steps": K, "warmup": Wm,
         "tokens_per_step": tokens, "closed_form_tokens_per_step": tok_closed,
         "target_step_us": t_target, "draft_token_us": t_draft, "loop_step_us": t_step,
-        "verify_us": t_step - gamma * t_draft,
-        "config": {"workload": args.workload, "B": B, "d": d, "V": V, "temperature": T},
+        "verify_us": t_verify, "verify_cost_target_steps": t_verify / t_target,
+        "config": {"workload": workload, "B": B, "d": d, "V": V, "temperature": T},
     }
-    print(json.dumps(line), flush=True)
+
+
+def run_loop(args):
+    """Prints loop_measure's line for --loop-c."""
+    print(json.dumps(loop_measure(args.workload, args.loop_c, args.steps, args.warmup,
+                                  args.seed)), flush=True)
 
 
 def run_gamma_sweep(args):

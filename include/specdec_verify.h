@@ -82,6 +82,10 @@ extern "C" {
  * workspace must be 256-byte aligned; its contents need no initialisation
  * and are overwritten by every call. Calls that share a workspace must be
  * ordered (same stream, or synchronised). Returns 0 for invalid shapes.
+ * Takes the mode besides the shape: greedy mode keeps no fp32 logits, no
+ * draft-logit records and no sampler chunk sums (it never reads the draft
+ * logits), so its workspace is a small fraction of the sampling one (at
+ * B = 256 on the Llama-3-8B-shaped head, 0.2 GB instead of 1.1 GB).
  */
 size_t specdec_verify_workspace_size(int B, int gamma, int d, int V, int dtype, int mode);
 
@@ -113,7 +117,11 @@ int specdec_verify(const void* hidden, const void* W_lm, const int32_t* draft_to
  *   lse_q      [B*gamma]    log sum_v exp(draft_logit_v / T) (sampling mode)
  *   p_x, q_x   [B*gamma]    p_i(x_i) and q_i(x_i)            (sampling mode)
  *   argmax_out [M]   int32  argmax_v z (lowest v among equal maxima)
- * Same results as specdec_verify() for the same inputs and seed.
+ * Same results as specdec_verify() for the same inputs and seed. There is
+ * no first-reject output: n_accepted already is that position (the first
+ * rejected draft sits at index n_accepted, or none when it equals gamma).
+ * The per-row argmax takes its place, since greedy parity needs the argmax
+ * of every scored row, not only of the rows the walk reached.
  */
 int specdec_verify_debug(const void* hidden, const void* W_lm, const int32_t* draft_tokens,
                          const void* draft_logits, int B, int gamma, int d, int V, int dtype,
@@ -177,7 +185,15 @@ int specdec_verify_host(const void* hidden_host, const void* W_lm, const int32_t
  * array and each clears what must start at zero, but calls whose work
  * overlaps on the GPU (different streams, or different host threads
  * without ordering) race on it and must be serialised by the caller.
- * specdec_read_status() does not apply: the status word lives in the array.
+ * specdec_read_status() does not apply: the status word lives in the array,
+ * so the exact device-side error code cannot be read. A step that failed
+ * on the device (a draft token outside [0, V), or a wait that ran out)
+ * shows in its outputs instead: n_accepted[b] = -1 and out_tokens[b, :] =
+ * -1 for every affected sequence (for a timeout, every sequence). The
+ * array's address is looked up again whenever the current context changes
+ * (after cudaDeviceReset, or with another context current on the device),
+ * so a reset does not leave the call writing through a stale address; that
+ * look-up, too, is best made before any stream capture.
  */
 #define SPECDEC_NOALLOC_SCRATCH_BYTES (16u << 20)
 int specdec_verify_noalloc(const void* hidden, const void* W_lm, const int32_t* draft_tokens,

@@ -9,6 +9,8 @@
 // For them the scratch lives in a file-scope __device__ array of
 // SPECDEC_NOALLOC_SCRATCH_BYTES, which every GPU that loads the library
 // holds until the process exits.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "kernels.h"
@@ -18,23 +20,65 @@ namespace {
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SPECDEC_NOALLOC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {nullptr};
 
-// Device address of the scratch array on the current device. The array's
-// name in host code is only a host-side stand-in, so the address is looked
-// up once per device, with that device current.
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// The driver's identity of the context current on this thread: 0 when it
+// cannot be told (no context yet, or the driver lacks the calls). Context
+// IDs are unique for the life of the process, so a context created after a
+// reset never matches one from before it.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa) ==
+            cudaSuccess &&
+        qa == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb) ==
+            cudaSuccess &&
+        qb == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(b);
+  });
+  CUcontext ctx = nullptr;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  unsigned long long id = 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+struct ScratchEntry {
+  unsigned long long ctx_id;   // context the address belongs to (0: unknown)
+  void* addr;
+};
+std::mutex g_mu;
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// Device address of the scratch array in the context current on this
+// thread. The array's name in host code is only a host-side stand-in, so
+// the address is looked up (cudaGetSymbolAddress) with the device current,
+// once per device and context: a reset or another context loads the module
+// anew, and the array may then sit elsewhere.
 int scratch_on_current_device(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SPECDEC_ERR_CUDA;
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_addr[dev] == nullptr) {
+  ScratchEntry& e = g_scratch[dev];
+  const unsigned long long id = current_context_id();
+  if (e.addr == nullptr || id == 0 || e.ctx_id != id) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
       return SPECDEC_ERR_CUDA;
-    g_scratch_addr[dev] = p;
+    e.addr = p;
+    // The look-up creates the context if there was none yet: take its ID now.
+    e.ctx_id = current_context_id();
   }
-  *out = g_scratch_addr[dev];
+  *out = e.addr;
   return SPECDEC_OK;
 }
 

@@ -227,6 +227,34 @@ __device__ __forceinline__ PartialQ q_chunk_stats(const __nv_bfloat16* __restric
   return PartialQ{m, s};
 }
 
+// One stage's MMAs: KC slices of four k16 steps. The descriptors advance by
+// constant offsets from the stage's first A and B descriptors (a shared
+// memory descriptor's low field is the byte address / 16), so the issue loop
+// spends a few instructions per MMA: one thread issues every MMA of the CTA
+// (or pair), and on shapes with narrow token tiles each MMA's tensor work is
+// short enough that the issue rate, not the tensor core, would otherwise set
+// the pace. Only the first MMA of a piece starts the accumulator afresh.
+template <int KC, bool kPair, bool kRowOwn>
+__device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t ad, uint64_t bd,
+                                            uint32_t b_slice16, uint32_t idesc,
+                                            uint32_t first_accum) {
+#pragma unroll
+  for (int c = 0; c < KC; ++c) {
+#pragma unroll
+    for (int k = 0; k < kBlockK / 16; ++k) {
+      const uint64_t a = ad + (uint64_t)(c * (kStageA >> 4) + 2 * k);
+      const uint64_t b = bd + (uint64_t)(c * b_slice16 + 2 * k);
+      const uint32_t accum = (c == 0 && k == 0) ? first_accum : 1u;
+      if constexpr (kRowOwn)   // A = token rows, B = W rows
+        tc2_mma_bf16(d_tmem, b, a, idesc, accum);
+      else if constexpr (kPair)
+        tc2_mma_bf16(d_tmem, a, b, idesc, accum);
+      else
+        tc_mma_bf16(d_tmem, a, b, idesc, accum);
+    }
+  }
+}
+
 __device__ __forceinline__ bool mbar_wait_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
   while (!mbar_try_wait(bar, parity)) {
@@ -381,7 +409,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         // ---------------------------------------------------- MMA issuer --
         const uint32_t idesc = idesc_bf16_f32(pair ? 2 * kBlockV : kBlockV, p.BT);
-        const int h_slice_bytes = hid_rows * kBlockK * 2;   // this CTA's rows of one slice
+        // Stage s, slice c: W rows [128 x 128 B] at sbase + s * stage_bytes + c * 16 KB,
+        // then this CTA's token rows [BT/K x 128 B] per slice after the kc W slices.
+        const uint64_t desc0 = smem_desc_sw128(sbase);
+        const uint32_t stage16 = p.stage_bytes >> 4;
+        const uint32_t hoff16 = (uint32_t)(p.kc * kStageA) >> 4;
+        const uint32_t hsl16 = (uint32_t)(hid_rows * kBlockK * 2) >> 4;
         int s = 0;
         uint32_t ph = 0;
         int ul = 0;
@@ -407,23 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a = sbase + (uint32_t)s * p.stage_bytes;
-            const uint32_t h = a + (uint32_t)(p.kc * kStageA);
-            for (int c = 0; c < p.kc; ++c) {
-              // slice c: W rows [128 x 128 B] at a + c*16 KB, token rows [BT/K x 128 B]
-              const uint64_t adesc = smem_desc_sw128(a + (uint32_t)(c * kStageA));
-              const uint64_t bdesc = smem_desc_sw128(h + (uint32_t)(c * h_slice_bytes));
-#pragma unroll
-              for (int k = 0; k < kBlockK / 16; ++k) {
-                const uint32_t accum = (kc > pc.kb || c > 0 || k > 0) ? 1u : 0u;
-                if constexpr (kRowOwn)   // A = token rows, B = W rows
-                  tc2_mma_bf16(d_tmem, bdesc + 2u * k, adesc + 2u * k, idesc, accum);
-                else if constexpr (kPair)
-                  tc2_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accum);
-                else
-                  tc_mma_bf16(d_tmem, adesc + 2u * k, bdesc + 2u * k, idesc, accum);
-              }
-            }
+            const uint64_t ad = desc0 + (uint64_t)((uint32_t)s * stage16);
+            const uint64_t bd = ad + hoff16;
+            const uint32_t fa = kc > pc.kb ? 1u : 0u;
+            if (p.kc == 4)
+              issue_stage<4, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, fa);
+            else if (p.kc == 2)
+              issue_stage<2, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, fa);
+            else
+              issue_stage<1, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, fa);
             if constexpr (kPair)
               tc2_commit_mc(empty_bar(s), 3);   // the stage is free in both CTAs
             else

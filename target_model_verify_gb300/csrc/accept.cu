@@ -16,8 +16,9 @@
 // the draw that follows and changes the drawn token for a share of the
 // uniforms equal to the summed boundary shifts. The fold therefore takes
 // the row maximum first and then adds the records' sums, each rescaled to
-// that maximum, in fp64: the fp32 rounding of each record stays random
-// and averages out instead of compounding through repeated rescaling.
+// that maximum, as error-free fp32 (hi, lo) pairs, combined in fp64 at the
+// end: the fp32 rounding of each record stays random and averages out
+// instead of compounding through repeated rescaling.
 #include "kernels.h"
 
 namespace specdec {
@@ -57,7 +58,7 @@ __device__ __forceinline__ void fold_row(const Rec* __restrict__ row, int n, flo
   }
   m = warp_max(m);
   if constexpr (kArgmax) warp_argmax(av, ai);
-  double s = 0.0;
+  float hi = 0.f, lo = 0.f;
   if (m != -INFINITY) {
     for (int base = lane; base < n; base += 32 * kBatch) {
       Rec x[kBatch];
@@ -70,11 +71,12 @@ __device__ __forceinline__ void fold_row(const Rec* __restrict__ row, int n, flo
       for (int u = 0; u < kBatch; ++u) {
         const int t = base + 32 * u;
         if (t < n && x[u].m != -INFINITY && x[u].s > 0.f)
-          s += (double)x[u].s * (double)exp2f((x[u].m - m) * c);
+          pair_add(hi, lo, x[u].s * exp2f((x[u].m - m) * c), 0.f);
       }
     }
   }
-  s_out = warp_sum_d(s);
+  warp_sum_pair(hi, lo);
+  s_out = (double)hi + (double)lo;
   m_out = m;
 }
 

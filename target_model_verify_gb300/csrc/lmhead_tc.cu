@@ -356,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int vt = (pc.unit / p.n_tt) * p.K + rank;
         const int tt = pc.unit % p.n_tt;
         for (int kc = pc.kb; kc < pc.ke; ++kc) {
-          const bool got = pair ? mbar_wait_cluster(empty_bar(s), ph ^ 1u, abort_flag, p.status)
-                                : mbar_wait(empty_bar(s), ph ^ 1u, abort_flag, p.status);
+          const bool got = pair ? mbar_wait_cluster<true>(empty_bar(s), ph ^ 1u, abort_flag, p.status)
+                                : mbar_wait<true>(empty_bar(s), ph ^ 1u, abort_flag, p.status);
           if (!got) {
             ok = false;
             break;
@@ -424,8 +424,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (ok && itr.next(p, pc)) {
           const int acc = ul & 1;
           const uint32_t aph = (uint32_t)(ul >> 1) & 1u;
-          const bool empty_ok = pair ? mbar_wait_cluster(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)
-                                     : mbar_wait(tempty_bar(acc), aph ^ 1u, abort_flag, p.status);
+          const bool empty_ok = pair ? mbar_wait_cluster<true>(tempty_bar(acc), aph ^ 1u, abort_flag, p.status)
+                                     : mbar_wait<true>(tempty_bar(acc), aph ^ 1u, abort_flag, p.status);
           if (!empty_ok) {
             ok = false;
             break;
@@ -433,8 +433,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.BT);
           for (int kc = pc.kb; kc < pc.ke; ++kc) {
-            const bool got = pair ? mbar_wait_cluster(full_bar(s), ph, abort_flag, p.status)
-                                  : mbar_wait(full_bar(s), ph, abort_flag, p.status);
+            const bool got = pair ? mbar_wait_cluster<true>(full_bar(s), ph, abort_flag, p.status)
+                                  : mbar_wait<true>(full_bar(s), ph, abort_flag, p.status);
             if (!got) {
               ok = false;
               break;
@@ -579,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int tt = pc.unit % p.n_tt;
       m = tt * p.BT + rank * 128 + r;
       if (threadIdx.x == 64)
-        *epi_flag = (mbar_wait_cluster(tfull_bar(acc), aph, abort_flag, p.status)) ? 1 : 0;
+        *epi_flag = (mbar_wait_cluster<true>(tfull_bar(acc), aph, abort_flag, p.status)) ? 1 : 0;
       named_bar_sync(1, kEpiThreads);
       const bool ok = *epi_flag != 0;
       named_bar_sync(2, kEpiThreads);
@@ -735,8 +735,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int v = vt * kBlockV + row;
       const int m_base = tt * p.BT;
       if (epi_tid == 0)
-        *epi_flag = (pair ? mbar_wait_cluster(tfull_bar(acc), aph, abort_flag, p.status)
-                          : mbar_wait(tfull_bar(acc), aph, abort_flag, p.status))
+        *epi_flag = (pair ? mbar_wait_cluster<true>(tfull_bar(acc), aph, abort_flag, p.status)
+                          : mbar_wait<true>(tfull_bar(acc), aph, abort_flag, p.status))
                         ? 1
                         : 0;
       named_bar_sync(1, kEpiThreads);

@@ -93,8 +93,8 @@ __device__ __forceinline__ void weights4(const Raw4& r, const SelectedRow& sr, b
 }
 
 // Sum of one chunk's weights: four coalesced sweeps, thread-sequential in
-// fp32, then warp shuffles and the 8 warp sums in order, in fp64. Every
-// thread returns the chunk total.
+// fp32, then an error-free (hi, lo) warp reduction and the 8 warp sums in
+// order in fp64 by thread 0. The total is valid in thread 0 only.
 template <typename DL>
 __device__ __forceinline__ double chunk_total(const float* zr, const DL* qr, const SelectedRow& sr,
                                               bool residual, float c, int V, bool vec, int chunk,
@@ -111,13 +111,15 @@ __device__ __forceinline__ double chunk_total(const float* zr, const DL* qr, con
 #pragma unroll
     for (int e = 0; e < kVec; ++e) ts += w[e];
   }
-  const double tsd = warp_sum_d((double)ts);
+  float hi = ts, lo = 0.f;
+  warp_sum_pair(hi, lo);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
-  if (lane == 0) red[warp] = tsd;
+  if (lane == 0) red[warp] = (double)hi + (double)lo;
   __syncthreads();
   double t = 0.0;
-  for (int i = 0; i < kSampleThreads / 32; ++i) t += red[i];
+  if (threadIdx.x == 0)
+    for (int i = 0; i < kSampleThreads / 32; ++i) t += red[i];
   return t;
 }
 
@@ -248,20 +250,30 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   float ts = 0.f;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) ts += w[k];
-  double incl = (double)ts;
+  // Inclusive warp scan of (hi, lo) pairs, then the warps' totals in fp64.
+  float ihi = ts, ilo = 0.f;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const double y = __shfl_up_sync(0xffffffffu, incl, o);
-    if (lane >= o) incl += y;
+    const float h2 = __shfl_up_sync(0xffffffffu, ihi, o);
+    const float l2 = __shfl_up_sync(0xffffffffu, ilo, o);
+    if (lane >= o) pair_add(ihi, ilo, h2, l2);
   }
-  double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-  if (lane == 0) excl = 0.0;
-  if (lane == 31) wscan[warp] = incl;
+  float ehi = __shfl_up_sync(0xffffffffu, ihi, 1);
+  float elo = __shfl_up_sync(0xffffffffu, ilo, 1);
+  if (lane == 0) ehi = elo = 0.f;
+  if (lane == 31) wscan[warp] = (double)ihi + (double)ilo;
   __syncthreads();
-  double wbefore = 0.0;
-  for (int i = 0; i < warp; ++i) wbefore += wscan[i];
+  if (tid == 0) {
+    double run_w = s_before;
+    for (int i = 0; i < kSampleThreads / 32; ++i) {
+      const double x = wscan[i];
+      wscan[i] = run_w;            // offset of warp i's first token
+      run_w += x;
+    }
+  }
+  __syncthreads();
   // This thread's tokens against t measured from the thread's first token.
-  const float t_loc = (float)(s_t - (s_before + (wbefore + excl)));
+  const float t_loc = (float)(s_t - (wscan[warp] + (double)ehi + (double)elo));
   float run = 0.f;
   int cand = 0x7fffffff, lastp = -1;
 #pragma unroll

@@ -10,15 +10,6 @@
 // Each warp folds the per-tile partials of one row into (max, sum) -- the
 // log-normaliser of z/T -- and the row's argmax; warp 0 then tests the
 // gamma guesses in parallel and finds the first rejection with a ballot.
-//
-// Precision: with a vocabulary of 10^5 tokens every token owns a CDF
-// interval of ~1e-5, so any error in the normalisers moves the boundaries of
-// the draw that follows and changes the drawn token for a share of the
-// uniforms equal to the summed boundary shifts. The fold therefore takes
-// the row maximum first and then adds the records' sums, each rescaled to
-// that maximum, as error-free fp32 (hi, lo) pairs, combined in fp64 at the
-// end: the fp32 rounding of each record stays random and averages out
-// instead of compounding through repeated rescaling.
 #include "kernels.h"
 
 namespace specdec {
@@ -27,67 +18,12 @@ namespace {
 constexpr int kThreads = 512;   // one warp per record row: up to 2*32+1 rows in one round
 constexpr int kBatch = 8;
 
-// (max, fp64 sum of exp2((z - max) c)) of one row's n records (PartialP or
-// PartialQ); every lane of the warp returns the row's values. With kArgmax
-// the records' (value, lowest index) argmax is folded alongside.
-template <typename Rec, bool kArgmax>
-__device__ __forceinline__ void fold_row(const Rec* __restrict__ row, int n, float c, float& m_out,
-                                         double& s_out, float& av, int& ai) {
-  const int lane = threadIdx.x & 31;
-  float m = -INFINITY;
-  for (int base = lane; base < n; base += 32 * kBatch) {
-    Rec x[kBatch];
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int t = base + 32 * u;
-      if (t < n) x[u] = row[t];
-    }
-#pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int t = base + 32 * u;
-      if (t < n) {
-        m = fmaxf(m, x[u].m);
-        if constexpr (kArgmax) {
-          if (argmax_better(x[u].amax_v, x[u].amax_i, av, ai)) {
-            av = x[u].amax_v;
-            ai = x[u].amax_i;
-          }
-        }
-      }
-    }
-  }
-  m = warp_max(m);
-  if constexpr (kArgmax) warp_argmax(av, ai);
-  float hi = 0.f, lo = 0.f;
-  if (m != -INFINITY) {
-    for (int base = lane; base < n; base += 32 * kBatch) {
-      Rec x[kBatch];
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int t = base + 32 * u;
-        if (t < n) x[u] = row[t];
-      }
-#pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int t = base + 32 * u;
-        if (t < n && x[u].m != -INFINITY && x[u].s > 0.f)
-          pair_add(hi, lo, x[u].s * exp2f((x[u].m - m) * c), 0.f);
-      }
-    }
-  }
-  warp_sum_pair(hi, lo);
-  s_out = (double)hi + (double)lo;
-  m_out = m;
-}
-
 template <typename DL>
 __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) {
-  __shared__ float s_pm[SPECDEC_MAX_GAMMA + 1];
-  __shared__ double s_ps[SPECDEC_MAX_GAMMA + 1];
+  __shared__ float s_pm[SPECDEC_MAX_GAMMA + 1], s_ps[SPECDEC_MAX_GAMMA + 1];
   __shared__ float s_am[SPECDEC_MAX_GAMMA + 1];
   __shared__ int s_ai[SPECDEC_MAX_GAMMA + 1];
-  __shared__ float s_qm[SPECDEC_MAX_GAMMA];
-  __shared__ double s_qs[SPECDEC_MAX_GAMMA];
+  __shared__ float s_qm[SPECDEC_MAX_GAMMA], s_qs[SPECDEC_MAX_GAMMA];
 
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -114,12 +50,36 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
   }
 
   for (int r = warp; r < rows; r += kThreads / 32) {
-    float m;
-    double s;
+    float m = -INFINITY, s = 0.f;
     if (r < g1) {
+      const PartialP* row = a.pp + (size_t)(b * g1 + r) * a.P;
       float av = -INFINITY;
       int ai = 0x7fffffff;
-      fold_row<PartialP, true>(a.pp + (size_t)(b * g1 + r) * a.P, a.P, a.c, m, s, av, ai);
+      // Records t = lane, lane+32, ... folded in that order; kBatch loads
+      // are issued before their merges so they overlap in flight.
+      for (int base = lane; base < a.P; base += 32 * kBatch) {
+        PartialP x[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int t = base + 32 * u;
+          x[u] = t < a.P ? row[t] : PartialP{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          if (sample) softmax_merge(m, s, x[u].m, x[u].s, a.c);
+          if (argmax_better(x[u].amax_v, x[u].amax_i, av, ai)) {
+            av = x[u].amax_v;
+            ai = x[u].amax_i;
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        softmax_merge(m, s, m2, s2, a.c);
+      }
+      warp_argmax(av, ai);
       if (lane == 0) {
         s_pm[r] = m;
         s_ps[r] = s;
@@ -128,9 +88,23 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
       }
     } else {
       const int i = r - g1;
-      float av = 0.f;
-      int ai = 0;
-      fold_row<PartialQ, false>(a.pq + ((size_t)b * gamma + i) * a.Pq, a.Pq, a.c, m, s, av, ai);
+      const PartialQ* row = a.pq + ((size_t)b * gamma + i) * a.Pq;
+      for (int base = lane; base < a.Pq; base += 32 * kBatch) {
+        PartialQ x[kBatch];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int t = base + 32 * u;
+          x[u] = t < a.Pq ? row[t] : PartialQ{-INFINITY, 0.f};
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) softmax_merge(m, s, x[u].m, x[u].s, a.c);
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+        softmax_merge(m, s, m2, s2, a.c);
+      }
       if (lane == 0) {
         s_qm[i] = m;
         s_qs[i] = s;
@@ -150,13 +124,14 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
     } else if (!sample) {
       rej = x != s_ai[lane];
     } else {
-      // p(x) and q(x) from the fp64 sums; the test r q <= p in fp64.
-      const double px = (double)exp2f((s_zx[lane] - s_pm[lane]) * a.c) / s_ps[lane];
-      const double qx = (double)exp2f((s_zqx[lane] - s_qm[lane]) * a.c) / s_qs[lane];
-      const double r = (double)accept_uniform(a.seed, b, lane);
+      const float zx = s_zx[lane];
+      const float zqx = s_zqx[lane];
+      const float px = exp2f((zx - s_pm[lane]) * a.c - log2f(s_ps[lane]));
+      const float qx = exp2f((zqx - s_qm[lane]) * a.c - log2f(s_qs[lane]));
+      const float r = accept_uniform(a.seed, b, lane);
       rej = !(r * qx <= px);
-      if (a.p_x) a.p_x[b * gamma + lane] = (float)px;
-      if (a.q_x) a.q_x[b * gamma + lane] = (float)qx;
+      if (a.p_x) a.p_x[b * gamma + lane] = px;
+      if (a.q_x) a.q_x[b * gamma + lane] = qx;
     }
   }
   const unsigned bad_mask = __ballot_sync(0xffffffffu, bad);
@@ -172,23 +147,21 @@ __global__ void __launch_bounds__(kThreads) accept_kernel(const AcceptLaunch a) 
     else if (i == j) t = sample ? -1 : s_ai[j];   // sampling: written by the sampler
     else t = -1;
     a.out_tokens[b * g1 + i] = t;
-    if (a.lse_p && sample)
-      a.lse_p[b * g1 + i] = (float)(((double)s_pm[i] * a.c + log2(s_ps[i])) * (double)kLn2);
+    if (a.lse_p && sample) a.lse_p[b * g1 + i] = (s_pm[i] * a.c + log2f(s_ps[i])) * kLn2;
     if (a.argmax_out) a.argmax_out[b * g1 + i] = s_ai[i];
   }
   if (a.lse_q && sample)
     for (int i = lane; i < gamma; i += 32)
-      a.lse_q[b * gamma + i] = (float)(((double)s_qm[i] * a.c + log2(s_qs[i])) * (double)kLn2);
+      a.lse_q[b * gamma + i] = (s_qm[i] * a.c + log2f(s_qs[i])) * kLn2;
   if (lane == 0) {
     a.n_accepted[b] = failed ? -1 : j;
     if (sample) {
       SelectedRow sr;
       sr.mp = s_pm[j];
+      sr.lsp = log2f(s_ps[j]);
       sr.residual = j < gamma ? 1 : 0;
       sr.mq = j < gamma ? s_qm[j] : 0.f;
-      const double R = j < gamma ? s_ps[j] / s_qs[j] : 0.0;
-      sr.r_hi = (float)R;
-      sr.r_lo = (float)(R - (double)sr.r_hi);
+      sr.lsq = j < gamma ? log2f(s_qs[j]) : 0.f;
       sr.j = failed ? -1 : j;
       sr.pad[0] = sr.pad[1] = 0;
       a.sel[b] = sr;

@@ -60,7 +60,7 @@ Plan make_plan(int B, int gamma, int d, int V, int dtype, int mode) {
   p.off_z = off;
   if (sample) off = align_up(off + sizeof(float) * (size_t)p.M * V);
   p.off_chunks = off;
-  if (sample) off = align_up(off + sizeof(double) * (size_t)B * p.nchunks);
+  if (sample) off = align_up(off + sizeof(float) * (size_t)B * p.nchunks);
   p.off_fix = off;
   if (dtype == SPECDEC_BF16) off = align_up(off + sizeof(float) * tc_fix_floats(p.M, V, d));
   p.total = off;
@@ -242,7 +242,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   PartialP* pp = reinterpret_cast<PartialP*>(ws + pl.off_pp);
   PartialQ* pq = reinterpret_cast<PartialQ*>(ws + pl.off_pq);
   float* z = ex.logits_out ? ex.logits_out : (sample ? reinterpret_cast<float*>(ws + pl.off_z) : nullptr);
-  double* chunk_sums = reinterpret_cast<double*>(ws + pl.off_chunks);
+  float* chunk_sums = reinterpret_cast<float*>(ws + pl.off_chunks);
   const float c = sample ? kLog2e / T : kLog2e;
 
   // Nothing is cleared up front: the LM-head kernel resets the status word

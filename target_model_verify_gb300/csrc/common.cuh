@@ -37,17 +37,10 @@ struct PartialQ {
   float m;
   float s;
 };
-// What the sampler needs about the row each sequence samples from. The
-// draw only needs the weights up to one common factor, so with
-// e_p(v) = exp2((z_v - mp) c) and e_q(v) = exp2((zq_v - mq) c) it uses
-// w(v) = e_p(v) (bonus) or max(0, e_p(v) - R e_q(v)) (residual), where
-// R = s_p / s_q is the ratio of the two rows' exp2 sums, held as an
-// unevaluated fp32 pair r_hi + r_lo so that the balance of p against q
-// keeps fp64 accuracy.
+// What the sampler needs about the row each sequence samples from.
 struct SelectedRow {
-  float mp;           // max z of target row j
-  float mq;           // max draft logit of draft row j (residual case)
-  float r_hi, r_lo;   // R = r_hi + r_lo (residual case)
+  float mp, lsp;      // max z and log2 of its sum, row j of the target
+  float mq, lsq;      // the same for the draft row j (residual case)
   int residual;       // 1: w = max(0, p - q); 0: w = p (bonus)
   int j;              // the position sampled (n_accepted), or -1: nothing to draw
   int pad[2];
@@ -129,37 +122,6 @@ __device__ __forceinline__ float warp_max(float x) {
   return x;
 }
 __device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-  return x;
-}
-// Error-free fp32 addition (Knuth's TwoSum): s + e == a + b exactly, with
-// s = fl(a + b). Carrying (hi, lo) pairs through a reduction keeps its
-// result accurate to about fp32 squared at fp32 speed (GB300's fp64 rate is
-// a small fraction of its fp32 rate, so wide fp64 reductions cost more than
-// the memory traffic they summarise).
-__device__ __forceinline__ void two_sum(float a, float b, float& s, float& e) {
-  s = a + b;
-  const float bb = s - a;
-  e = (a - (s - bb)) + (b - bb);
-}
-// (hi, lo) += (h2, l2)
-__device__ __forceinline__ void pair_add(float& hi, float& lo, float h2, float l2) {
-  float s, e;
-  two_sum(hi, h2, s, e);
-  hi = s;
-  lo = lo + l2 + e;
-}
-// Sum over the warp of (hi, lo) pairs; every lane gets the pair.
-__device__ __forceinline__ void warp_sum_pair(float& hi, float& lo) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float h2 = __shfl_xor_sync(0xffffffffu, hi, o);
-    const float l2 = __shfl_xor_sync(0xffffffffu, lo, o);
-    pair_add(hi, lo, h2, l2);
-  }
-}
-__device__ __forceinline__ double warp_sum_d(double x) {
 #pragma unroll
   for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
   return x;

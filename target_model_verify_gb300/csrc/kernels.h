@@ -69,7 +69,7 @@ struct SampleLaunch {
   const float* z;
   const void* dl;
   const SelectedRow* sel;
-  double* chunk_sums;          // [B, nchunks] fp64 chunk weight sums
+  float* chunk_sums;
   int* counters;
   int32_t* out_tokens;
 };

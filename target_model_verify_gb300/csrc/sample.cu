@@ -14,16 +14,6 @@
 // sequence to finish (atomic ticket, no waiting) forms the prefix of the
 // chunk sums with one warp, finds the chunk holding t, rescans that chunk in
 // token order (16 contiguous tokens per thread) and writes the token.
-//
-// Precision: with ~10^5 tokens each token's interval is ~1e-5 of the unit
-// range, and any error in the boundaries C_v / S changes the drawn token
-// for that share of the uniforms. So the weights are taken up to a common
-// factor (no fp32 normaliser: bonus w = e_p, residual w = max(0, e_p -
-// R e_q) with the p/q balance R as an fp32 pair applied by two fused
-// multiply-adds), each thread's 16 weights are summed in fp32 and everything
-// above that -- chunk sums, their prefix, the target t and each thread's
-// offset -- in fp64. The rescan compares each thread's own fp32 running sum
-// with t minus the thread's fp64 offset.
 #include "kernels.h"
 
 namespace specdec {
@@ -73,32 +63,29 @@ __device__ __forceinline__ Raw4 load4(const float* __restrict__ zr, const DL* __
   return r;
 }
 
-// w = max(0, e_p - R e_q) (residual) or e_p (bonus), for the four tokens
-// of a group, e_p = exp2((z - mp) c), e_q = exp2((zq - mq) c).
+// w = max(0, p - q) (residual) or p, for the four tokens of a group.
 __device__ __forceinline__ void weights4(const Raw4& r, const SelectedRow& sr, bool residual,
                                          float c, float* w) {
   const float zz[kVec] = {r.z.x, r.z.y, r.z.z, r.z.w};
 #pragma unroll
   for (int e = 0; e < kVec; ++e) {
-    const float ep = exp2f((zz[e] - sr.mp) * c);
+    const float p = exp2f((zz[e] - sr.mp) * c - sr.lsp);
     if (residual) {
-      const float eq = exp2f((r.q[e] - sr.mq) * c);
-      // R e_q - e_p with R = r_hi + r_lo: one rounding for the main term.
-      const float d = fmaf(eq, sr.r_lo, fmaf(eq, sr.r_hi, -ep));
-      w[e] = fmaxf(0.f, -d);
+      const float qv = exp2f((r.q[e] - sr.mq) * c - sr.lsq);
+      w[e] = fmaxf(0.f, p - qv);
     } else {
-      w[e] = ep;
+      w[e] = p;
     }
   }
 }
 
-// Sum of one chunk's weights: four coalesced sweeps, thread-sequential in
-// fp32, then an error-free (hi, lo) warp reduction and the 8 warp sums in
-// order in fp64 by thread 0. The total is valid in thread 0 only.
+// Sum of one chunk's weights: four coalesced sweeps, thread-sequential,
+// then warp shuffles, then the 8 warp sums in order. Every thread returns
+// the chunk total.
 template <typename DL>
-__device__ __forceinline__ double chunk_total(const float* zr, const DL* qr, const SelectedRow& sr,
-                                              bool residual, float c, int V, bool vec, int chunk,
-                                              double* red) {
+__device__ __forceinline__ float chunk_total(const float* zr, const DL* qr, const SelectedRow& sr,
+                                             bool residual, float c, int V, bool vec, int chunk,
+                                             float* red) {
   const int v0 = chunk * kChunkV + threadIdx.x * kVec;
   Raw4 raw[kSweeps];
 #pragma unroll
@@ -111,35 +98,33 @@ __device__ __forceinline__ double chunk_total(const float* zr, const DL* qr, con
 #pragma unroll
     for (int e = 0; e < kVec; ++e) ts += w[e];
   }
-  float hi = ts, lo = 0.f;
-  warp_sum_pair(hi, lo);
+  ts = warp_sum(ts);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   __syncthreads();
-  if (lane == 0) red[warp] = (double)hi + (double)lo;
+  if (lane == 0) red[warp] = ts;
   __syncthreads();
-  double t = 0.0;
-  if (threadIdx.x == 0)
-    for (int i = 0; i < kSampleThreads / 32; ++i) t += red[i];
+  float t = 0.f;
+  for (int i = 0; i < kSampleThreads / 32; ++i) t += red[i];
   return t;
 }
 
 // Warp 0: inclusive prefix of the chunk sums in chunk order (groups of 32,
-// fp64 shuffle scan, carried total), and the last chunk holding weight.
-__device__ __forceinline__ void prefix_chunks(const double* cs, double* pre, int n, int* last_pos) {
+// shuffle scan, carried total), and the last chunk holding weight.
+__device__ __forceinline__ void prefix_chunks(const float* cs, float* pre, int n, int* last_pos) {
   const int lane = threadIdx.x & 31;
-  double carry = 0.0;
+  float carry = 0.f;
   int lp = -1;
   for (int g = 0; g < n; g += 32) {
     const int k = g + lane;
-    const double x = k < n ? cs[k] : 0.0;
-    double incl = x;
+    const float x = k < n ? cs[k] : 0.f;
+    float incl = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const double y = __shfl_up_sync(0xffffffffu, incl, o);
+      const float y = __shfl_up_sync(0xffffffffu, incl, o);
       if (lane >= o) incl += y;
     }
     if (k < n) pre[k] = carry + incl;
-    const unsigned pos = __ballot_sync(0xffffffffu, k < n && x > 0.0);
+    const unsigned pos = __ballot_sync(0xffffffffu, k < n && x > 0.f);
     if (pos) lp = g + 31 - __clz(pos);
     carry += __shfl_sync(0xffffffffu, incl, 31);
   }
@@ -148,16 +133,16 @@ __device__ __forceinline__ void prefix_chunks(const double* cs, double* pre, int
 
 template <typename DL>
 __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaunch L) {
-  __shared__ double red[kSampleThreads / 32];
-  __shared__ double wscan[kSampleThreads / 32];
-  __shared__ double s_cs[kMaxChunks];
-  __shared__ double s_pre[kMaxChunks];
+  __shared__ float red[kSampleThreads / 32];
+  __shared__ float wscan[kSampleThreads / 32];
+  __shared__ float s_cs[kMaxChunks];
+  __shared__ float s_pre[kMaxChunks];
   __shared__ int s_last;
   __shared__ int s_tok;
   __shared__ int s_lastpos;
   __shared__ int s_lastchunk;
   __shared__ int s_chunk;
-  __shared__ double s_before, s_t;
+  __shared__ float s_before, s_t;
   __shared__ int s_residual;
 
   const int b = blockIdx.y;
@@ -188,7 +173,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
 
-  const double total = chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, vec, chunk, red);
+  const float total = chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, vec, chunk, red);
   if (tid == 0) {
     L.chunk_sums[(size_t)b * L.nchunks + chunk] = total;
     __threadfence();
@@ -200,18 +185,18 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   __threadfence();
 
   // ---- last CTA of sequence b: locate the chunk holding t = u * S ----
-  const double u = (double)sample_uniform(L.seed, b, sr.j);
+  const float u = sample_uniform(L.seed, b, sr.j);
   for (int k = tid; k < L.nchunks; k += kSampleThreads)
     s_cs[k] = __ldcg(L.chunk_sums + (size_t)b * L.nchunks + k);
   __syncthreads();
   if (warp == 0) prefix_chunks(s_cs, s_pre, L.nchunks, &s_lastchunk);
   __syncthreads();
   bool residual = sr.residual != 0;
-  if (residual && !(s_pre[L.nchunks - 1] > 0.0)) {
+  if (residual && !(s_pre[L.nchunks - 1] > 0.f)) {
     // p == q to rounding: draw from p. Recompute every chunk sum with w = p.
     residual = false;
     for (int k = 0; k < L.nchunks; ++k) {
-      const double tot = chunk_total<DL>(zr, qr, sr, false, L.c, L.V, vec, k, red);
+      const float tot = chunk_total<DL>(zr, qr, sr, false, L.c, L.V, vec, k, red);
       if (tid == 0) s_cs[k] = tot;
     }
     __syncthreads();
@@ -219,7 +204,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
     __syncthreads();
   }
   if (warp == 0) {
-    const double t = u * s_pre[L.nchunks - 1];
+    const float t = u * s_pre[L.nchunks - 1];
     int found = -1;
     for (int g = 0; g < L.nchunks && found < 0; g += 32) {
       const int k = g + lane;
@@ -230,7 +215,7 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
     if (found < 0) found = 0;             // no weight at all (cannot happen for w = p)
     if (lane == 0) {
       s_chunk = found;
-      s_before = found > 0 ? s_pre[found - 1] : 0.0;
+      s_before = found > 0 ? s_pre[found - 1] : 0.f;
       s_t = t;
       s_tok = 0x7fffffff;
       s_lastpos = -1;
@@ -250,37 +235,26 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   float ts = 0.f;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) ts += w[k];
-  // Inclusive warp scan of (hi, lo) pairs, then the warps' totals in fp64.
-  float ihi = ts, ilo = 0.f;
+  float incl = ts;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const float h2 = __shfl_up_sync(0xffffffffu, ihi, o);
-    const float l2 = __shfl_up_sync(0xffffffffu, ilo, o);
-    if (lane >= o) pair_add(ihi, ilo, h2, l2);
+    const float y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
   }
-  float ehi = __shfl_up_sync(0xffffffffu, ihi, 1);
-  float elo = __shfl_up_sync(0xffffffffu, ilo, 1);
-  if (lane == 0) ehi = elo = 0.f;
-  if (lane == 31) wscan[warp] = (double)ihi + (double)ilo;
+  float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+  if (lane == 0) excl = 0.f;
+  if (lane == 31) wscan[warp] = incl;
   __syncthreads();
-  if (tid == 0) {
-    double run_w = s_before;
-    for (int i = 0; i < kSampleThreads / 32; ++i) {
-      const double x = wscan[i];
-      wscan[i] = run_w;            // offset of warp i's first token
-      run_w += x;
-    }
-  }
-  __syncthreads();
-  // This thread's tokens against t measured from the thread's first token.
-  const float t_loc = (float)(s_t - (wscan[warp] + (double)ehi + (double)elo));
-  float run = 0.f;
+  float wbefore = 0.f;
+  for (int i = 0; i < warp; ++i) wbefore += wscan[i];
+  float run = s_before + (wbefore + excl);
+  const float t = s_t;
   int cand = 0x7fffffff, lastp = -1;
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     run += w[k];
     if (w[k] > 0.f) lastp = v0 + k;
-    if (cand == 0x7fffffff && w[k] > 0.f && run > t_loc) cand = v0 + k;
+    if (cand == 0x7fffffff && w[k] > 0.f && run > t) cand = v0 + k;
   }
   if (cand != 0x7fffffff) atomicMin(&s_tok, cand);
   if (lastp >= 0) atomicMax(&s_lastpos, lastp);

@@ -73,6 +73,10 @@ struct SampleLaunch {
   int* counters;
   int32_t* out_tokens;
 };
+// Up to kSampleOneKernelItems (sequence, chunk) pairs one kernel sums the
+// chunks and draws (the last CTA of each sequence to finish draws); beyond,
+// a kernel of chunk sums and a kernel of one drawing CTA per sequence.
+constexpr long long kSampleOneKernelItems = 608;
 cudaError_t launch_sample(const SampleLaunch& L, cudaStream_t stream);
 
 // Tree verification walk: one cluster of kTreeCluster CTAs per sequence

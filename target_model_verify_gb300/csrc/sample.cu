@@ -14,6 +14,11 @@
 // sequence to finish (atomic ticket, no waiting) forms the prefix of the
 // chunk sums with one warp, finds the chunk holding t, rescans that chunk in
 // token order (16 contiguous tokens per thread) and writes the token.
+// With many sequences (more than kSampleOneKernelItems (sequence, chunk)
+// pairs) the sums come from a kernel without tickets and one CTA per
+// sequence draws in a second kernel: the fence and atomic that the ticket
+// needs kept every summing CTA resident past its loads (measured: 79 ->
+// 74 us for accept and draw at batch 256, 35 -> 34 us at batch 64).
 #include "kernels.h"
 
 namespace specdec {
@@ -131,59 +136,37 @@ __device__ __forceinline__ void prefix_chunks(const float* cs, float* pre, int n
   if (lane == 0) *last_pos = lp;
 }
 
-template <typename DL>
-__global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaunch L) {
-  __shared__ float red[kSampleThreads / 32];
-  __shared__ float wscan[kSampleThreads / 32];
-  __shared__ float s_cs[kMaxChunks];
-  __shared__ float s_pre[kMaxChunks];
-  __shared__ int s_last;
-  __shared__ int s_tok;
-  __shared__ int s_lastpos;
-  __shared__ int s_lastchunk;
-  __shared__ int s_chunk;
-  __shared__ float s_before, s_t;
-  __shared__ int s_residual;
+// Shared memory of the draw (the last step of a sequence, one CTA).
+struct DrawSmem {
+  float red[kSampleThreads / 32];
+  float wscan[kSampleThreads / 32];
+  float s_cs[kMaxChunks];
+  float s_pre[kMaxChunks];
+  int s_tok, s_lastpos, s_lastchunk, s_chunk, s_residual;
+  float s_before, s_t;
+};
 
-  const int b = blockIdx.y;
-  const int chunk = blockIdx.x;
-  if (L.prefetch && threadIdx.x < 2 * (L.gamma + 1)) {
-    // Small batch: the row is not known yet, but every candidate row's chunk
-    // was written by the LM-head kernel, which finished before the
-    // acceptance kernel began; pull them into L2 while that kernel runs.
-    const int r = threadIdx.x >> 1;
-    const int v0 = chunk * kChunkV;
-    const int n = min(kChunkV, L.V - v0);
-    if (threadIdx.x & 1) {
-      if (r < L.gamma)
-        bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(L.dl) + ((size_t)b * L.gamma + r) * L.V + v0,
-                         (uint32_t)n * 2u);
-    } else {
-      bulk_prefetch_l2(L.z + ((size_t)b * (L.gamma + 1) + r) * L.V + v0, (uint32_t)n * 4u);
-    }
-  }
-  grid_dependency_wait();      // the acceptance kernel's selection is complete
-  const SelectedRow sr = L.sel[b];
-  if (sr.j < 0) return;
-  const int g1 = L.gamma + 1;
-  const float* zr = L.z + (size_t)(b * g1 + sr.j) * L.V;
-  const DL* qr = sr.residual ? static_cast<const DL*>(L.dl) + ((size_t)b * L.gamma + sr.j) * L.V
-                             : nullptr;
+// The draw of sequence b with the whole CTA, once every chunk sum of its
+// row is in L.chunk_sums: prefix of the chunk sums, the chunk holding
+// t = u * S, a rescan of that chunk in token order, the token.
+template <typename DL>
+__device__ __forceinline__ void draw_sequence(const SampleLaunch& L, int b, const SelectedRow& sr,
+                                              const float* zr, const DL* qr, DrawSmem& sm) {
+  float* red = sm.red;
+  float* wscan = sm.wscan;
+  float* s_cs = sm.s_cs;
+  float* s_pre = sm.s_pre;
+  int& s_tok = sm.s_tok;
+  int& s_lastpos = sm.s_lastpos;
+  int& s_lastchunk = sm.s_lastchunk;
+  int& s_chunk = sm.s_chunk;
+  int& s_residual = sm.s_residual;
+  float& s_before = sm.s_before;
+  float& s_t = sm.s_t;
   const bool vec = L.vec != 0;
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
-
-  const float total = chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, vec, chunk, red);
-  if (tid == 0) {
-    L.chunk_sums[(size_t)b * L.nchunks + chunk] = total;
-    __threadfence();
-    const int ticket = atomicAdd(&L.counters[b], 1);
-    s_last = ticket == L.nchunks - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-
+  const int g1 = L.gamma + 1;
   // ---- last CTA of sequence b: locate the chunk holding t = u * S ----
   const float u = sample_uniform(L.seed, b, sr.j);
   for (int k = tid; k < L.nchunks; k += kSampleThreads)
@@ -266,6 +249,87 @@ __global__ void __launch_bounds__(kSampleThreads) sample_kernel(const SampleLaun
   }
 }
 
+// Small batch: grid (chunks, B). Each CTA sums one chunk; the last CTA of a
+// sequence to finish (atomic ticket, no waiting) draws.
+template <typename DL>
+__global__ void __launch_bounds__(kSampleThreads, 6) sample_kernel(const SampleLaunch L) {
+  __shared__ DrawSmem sm;
+  __shared__ int s_last;
+
+  const int b = blockIdx.y;
+  const int chunk = blockIdx.x;
+  if (L.prefetch && threadIdx.x < 2 * (L.gamma + 1)) {
+    // Small batch: the row is not known yet, but every candidate row's chunk
+    // was written by the LM-head kernel, which finished before the
+    // acceptance kernel began; pull them into L2 while that kernel runs.
+    const int r = threadIdx.x >> 1;
+    const int v0 = chunk * kChunkV;
+    const int n = min(kChunkV, L.V - v0);
+    if (threadIdx.x & 1) {
+      if (r < L.gamma)
+        bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(L.dl) + ((size_t)b * L.gamma + r) * L.V + v0,
+                         (uint32_t)n * 2u);
+    } else {
+      bulk_prefetch_l2(L.z + ((size_t)b * (L.gamma + 1) + r) * L.V + v0, (uint32_t)n * 4u);
+    }
+  }
+  grid_dependency_wait();      // the acceptance kernel's selection is complete
+  const SelectedRow sr = L.sel[b];
+  if (sr.j < 0) return;
+  const int g1 = L.gamma + 1;
+  const float* zr = L.z + (size_t)(b * g1 + sr.j) * L.V;
+  const DL* qr = sr.residual ? static_cast<const DL*>(L.dl) + ((size_t)b * L.gamma + sr.j) * L.V
+                             : nullptr;
+  const float total =
+      chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, L.vec != 0, chunk, sm.red);
+  if (threadIdx.x == 0) {
+    L.chunk_sums[(size_t)b * L.nchunks + chunk] = total;
+    __threadfence();
+    const int ticket = atomicAdd(&L.counters[b], 1);
+    s_last = ticket == L.nchunks - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  draw_sequence<DL>(L, b, sr, zr, qr, sm);
+}
+
+// Many sequences: the same chunk sums without tickets (each CTA writes its
+// sum and leaves, so no CTA stays resident through a fence and an atomic),
+// then one CTA per sequence draws in a second kernel.
+template <typename DL>
+__global__ void __launch_bounds__(kSampleThreads, 6) sample_sums_kernel(const SampleLaunch L) {
+  __shared__ float red[kSampleThreads / 32];
+  const int b = blockIdx.y;
+  const int chunk = blockIdx.x;
+  // No early trigger of the draw kernel: its CTAs would sit on SMs the
+  // chunk sums need (measured slower at batch 64 and 256).
+  grid_dependency_wait();      // the acceptance kernel's selection is complete
+  const SelectedRow sr = L.sel[b];
+  if (sr.j < 0) return;
+  const int g1 = L.gamma + 1;
+  const float* zr = L.z + (size_t)(b * g1 + sr.j) * L.V;
+  const DL* qr = sr.residual ? static_cast<const DL*>(L.dl) + ((size_t)b * L.gamma + sr.j) * L.V
+                             : nullptr;
+  const float total =
+      chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, L.vec != 0, chunk, red);
+  if (threadIdx.x == 0) L.chunk_sums[(size_t)b * L.nchunks + chunk] = total;
+}
+
+template <typename DL>
+__global__ void __launch_bounds__(kSampleThreads) sample_draw_kernel(const SampleLaunch L) {
+  __shared__ DrawSmem sm;
+  const int b = blockIdx.x;
+  grid_dependency_wait();      // every chunk sum is written
+  const SelectedRow sr = L.sel[b];
+  if (sr.j < 0) return;
+  const int g1 = L.gamma + 1;
+  const float* zr = L.z + (size_t)(b * g1 + sr.j) * L.V;
+  const DL* qr = sr.residual ? static_cast<const DL*>(L.dl) + ((size_t)b * L.gamma + sr.j) * L.V
+                             : nullptr;
+  draw_sequence<DL>(L, b, sr, zr, qr, sm);
+}
+
 }  // namespace
 
 cudaError_t launch_sample(const SampleLaunch& L0, cudaStream_t stream) {
@@ -290,8 +354,16 @@ cudaError_t launch_sample(const SampleLaunch& L0, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (L.dl_bf16) return cudaLaunchKernelEx(&cfg, sample_kernel<__nv_bfloat16>, L);
-  return cudaLaunchKernelEx(&cfg, sample_kernel<float>, L);
+  if ((long long)L.B * L.nchunks <= kSampleOneKernelItems) {
+    if (L.dl_bf16) return cudaLaunchKernelEx(&cfg, sample_kernel<__nv_bfloat16>, L);
+    return cudaLaunchKernelEx(&cfg, sample_kernel<float>, L);
+  }
+  cudaError_t e = L.dl_bf16 ? cudaLaunchKernelEx(&cfg, sample_sums_kernel<__nv_bfloat16>, L)
+                            : cudaLaunchKernelEx(&cfg, sample_sums_kernel<float>, L);
+  if (e != cudaSuccess) return e;
+  cfg.gridDim = dim3(L.B);
+  if (L.dl_bf16) return cudaLaunchKernelEx(&cfg, sample_draw_kernel<__nv_bfloat16>, L);
+  return cudaLaunchKernelEx(&cfg, sample_draw_kernel<float>, L);
 }
 
 }  // namespace specdec

@@ -274,6 +274,11 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   const int Pq = q_stream ? (V + kQChunk - 1) / kQChunk : 0;
   ep.Pq = Pq;
   ep.q_vec = (V % 8 == 0 && ((uintptr_t)draft_logits & 15u) == 0) ? 1 : 0;
+  // Small batches draw in the same kernel as the acceptance test; its
+  // tickets are cleared by the LM-head kernel.
+  const bool fused = sample && fused_accept_sample(B, pl.nchunks);
+  ep.counters = fused ? counters : nullptr;
+  ep.n_counters = fused ? B : 0;
 
   if (ex.ev0 && cudaEventRecord(ex.ev0, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
   if (dtype == SPECDEC_BF16) {
@@ -312,7 +317,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   A.p_x = ex.p_x;
   A.q_x = ex.q_x;
   A.argmax_out = ex.argmax_out;
-  if (launch_accept(A, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+  if (!fused && launch_accept(A, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
 
   if (sample) {
     SampleLaunch S;
@@ -329,7 +334,8 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
     S.chunk_sums = chunk_sums;
     S.counters = counters;
     S.out_tokens = out_tokens;
-    if (launch_sample(S, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
+    const cudaError_t e = fused ? launch_accept_sample(A, S, stream) : launch_sample(S, stream);
+    if (e != cudaSuccess) return SPECDEC_ERR_CUDA;
   }
   return SPECDEC_OK;
 }
@@ -671,6 +677,8 @@ int specdec_selftest_wait_timeout(void* workspace, size_t workspace_bytes, void*
   ep.n_qrows = 0;
   ep.Pq = 0;
   ep.q_vec = 0;
+  ep.counters = nullptr;
+  ep.n_counters = 0;
   TcLaunch L;
   L.tmap_w = &tw;
   L.tmap_h = &th;
@@ -765,6 +773,8 @@ int specdec_verify_tree_timed(const void* hidden, const void* W_lm, const int32_
   ep.n_qrows = pl.M;
   ep.Pq = pl.Pq;
   ep.q_vec = (V % 8 == 0 && ((uintptr_t)draft_logits & 15u) == 0) ? 1 : 0;
+  ep.counters = nullptr;
+  ep.n_counters = 0;
   int P = 0;
   cudaEvent_t ev0 = static_cast<cudaEvent_t>(lmhead_start_event);
   cudaEvent_t ev1 = static_cast<cudaEvent_t>(lmhead_end_event);

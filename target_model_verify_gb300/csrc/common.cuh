@@ -726,6 +726,8 @@ struct EpiParams {
   int n_qrows;             // draft-logit rows the streamer reduces (rows of dl, in order)
   int Pq;                  // q records per draft row when streamed: ceil(V / kQChunk)
   int q_vec;               // streamed rows allow 16-byte loads (V % 8 == 0, aligned base)
+  int* counters;           // sampler tickets the LM-head kernel clears (fused draw), or NULL
+  int n_counters;
 };
 
 __device__ __forceinline__ void redslot_merge(RedSlot& a, const RedSlot& o, float c) {

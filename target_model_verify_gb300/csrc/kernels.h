@@ -78,6 +78,14 @@ struct SampleLaunch {
 // a kernel of chunk sums and a kernel of one drawing CTA per sequence.
 constexpr long long kSampleOneKernelItems = 608;
 cudaError_t launch_sample(const SampleLaunch& L, cudaStream_t stream);
+// Small batches in sampling mode: acceptance and draw in one kernel (every
+// drawing CTA folds its sequence's records itself). The sampler tickets
+// must be zero when it starts: the LM-head kernel clears them
+// (EpiParams::counters). kFusedAcceptItems bounds B * nchunks.
+constexpr long long kFusedAcceptItems = 128;
+bool fused_accept_sample(int B, int nchunks);
+cudaError_t launch_accept_sample(const AcceptLaunch& A, const SampleLaunch& L,
+                                 cudaStream_t stream);
 
 // Tree verification walk: one cluster of kTreeCluster CTAs per sequence
 // (sampling; the CTAs split the vocabulary), kTreeClusterWide when every

@@ -18,6 +18,8 @@ __global__ void __launch_bounds__(128)
                       const EpiParams ep, int* status) {
   grid_dependency_wait();
   if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) *(volatile int*)status = SPECDEC_OK;
+  if (blockIdx.x == 0 && blockIdx.y == 0)
+    for (int i = threadIdx.x; i < ep.n_counters; i += blockDim.x) ep.counters[i] = 0;
   __shared__ float ws[kKSlice][kBlockV + 1];
   __shared__ float hs[16][kKSlice];
   __shared__ RedSlot red[64];

@@ -330,6 +330,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the previous kernel; global memory is touched only after this wait.
   grid_dependency_wait();
   if (blockIdx.x == 0 && threadIdx.x == 0) *(volatile int*)p.status = SPECDEC_OK;
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < p.ep.n_counters; i += kThreads) p.ep.counters[i] = 0;
   // This call's fix-up tag; the call count only changes after this kernel.
   const unsigned long long tag = call_tag(p.epoch, p.calls);
   tc_fence_before();

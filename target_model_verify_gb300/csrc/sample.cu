@@ -19,7 +19,7 @@
 // sequence draws in a second kernel: the fence and atomic that the ticket
 // needs kept every summing CTA resident past its loads (measured: 79 ->
 // 74 us for accept and draw at batch 256, 35 -> 34 us at batch 64).
-#include "kernels.h"
+#include "accept.cuh"
 
 namespace specdec {
 namespace {
@@ -294,6 +294,62 @@ __global__ void __launch_bounds__(kSampleThreads, 6) sample_kernel(const SampleL
   draw_sequence<DL>(L, b, sr, zr, qr, sm);
 }
 
+// Small batch, acceptance fused in: grid (chunks, B). Every CTA folds its
+// sequence's records and takes the acceptance decision itself (the same
+// records in the same order, so every CTA of a sequence decides alike; the
+// chunk-0 CTA writes the kept prefix, n_accepted and the status), then sums
+// its chunk of the selected row, and the last CTA of the sequence to finish
+// (atomic ticket; the LM-head kernel zeroed the tickets) draws. One kernel
+// boundary fewer than acceptance kernel + sampler.
+template <typename DL>
+__global__ void __launch_bounds__(kSampleThreads) accept_sample_kernel(const AcceptLaunch A,
+                                                                       const SampleLaunch L) {
+  __shared__ DrawSmem sm;
+  __shared__ AcceptSmem asm_;
+  __shared__ int s_last;
+
+  const int b = blockIdx.y;
+  const int chunk = blockIdx.x;
+  if (L.prefetch && threadIdx.x < 2 * (L.gamma + 1)) {
+    // The row is not known yet, but every candidate row's chunk was written
+    // by the LM-head kernel: pull them into L2 while the records fold.
+    const int r = threadIdx.x >> 1;
+    const int v0 = chunk * kChunkV;
+    const int n = min(kChunkV, L.V - v0);
+    if (threadIdx.x & 1) {
+      if (r < L.gamma)
+        bulk_prefetch_l2(static_cast<const __nv_bfloat16*>(L.dl) + ((size_t)b * L.gamma + r) * L.V + v0,
+                         (uint32_t)n * 2u);
+    } else {
+      bulk_prefetch_l2(L.z + ((size_t)b * (L.gamma + 1) + r) * L.V + v0, (uint32_t)n * 4u);
+    }
+  }
+  grid_dependency_wait();      // the LM-head kernel's records are complete
+  if (b == 0 && chunk == 0 && threadIdx.x == 0) *A.calls += 1;   // the LM head of this call is done
+  accept_fold<DL>(A, b, asm_);
+  __syncthreads();
+  if (threadIdx.x < 32) accept_decide<DL>(A, b, asm_, chunk == 0);
+  __syncthreads();
+  const SelectedRow sr = asm_.sr;
+  if (sr.j < 0) return;
+  const int g1 = L.gamma + 1;
+  const float* zr = L.z + (size_t)(b * g1 + sr.j) * L.V;
+  const DL* qr = sr.residual ? static_cast<const DL*>(L.dl) + ((size_t)b * L.gamma + sr.j) * L.V
+                             : nullptr;
+  const float total =
+      chunk_total<DL>(zr, qr, sr, sr.residual != 0, L.c, L.V, L.vec != 0, chunk, sm.red);
+  if (threadIdx.x == 0) {
+    L.chunk_sums[(size_t)b * L.nchunks + chunk] = total;
+    __threadfence();
+    const int ticket = atomicAdd(&L.counters[b], 1);
+    s_last = ticket == L.nchunks - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  draw_sequence<DL>(L, b, sr, zr, qr, sm);
+}
+
 // Many sequences: the same chunk sums without tickets (each CTA writes its
 // sum and leaves, so no CTA stays resident through a fence and an atomic),
 // then one CTA per sequence draws in a second kernel.
@@ -332,7 +388,8 @@ __global__ void __launch_bounds__(kSampleThreads) sample_draw_kernel(const Sampl
 
 }  // namespace
 
-cudaError_t launch_sample(const SampleLaunch& L0, cudaStream_t stream) {
+namespace {
+SampleLaunch prepare_sample(const SampleLaunch& L0) {
   SampleLaunch L = L0;
   const uintptr_t dl_align = L.dl_bf16 ? 8 : 16;
   L.vec = (L.V % kVec == 0 && ((uintptr_t)L.z & 15u) == 0 &&
@@ -345,6 +402,32 @@ cudaError_t launch_sample(const SampleLaunch& L0, cudaStream_t stream) {
                 ((uintptr_t)L.dl & 15u) == 0)
                    ? 1
                    : 0;
+  return L;
+}
+}  // namespace
+
+bool fused_accept_sample(int B, int nchunks) {
+  return (long long)B * nchunks <= kFusedAcceptItems;
+}
+
+cudaError_t launch_accept_sample(const AcceptLaunch& A, const SampleLaunch& L0,
+                                 cudaStream_t stream) {
+  const SampleLaunch L = prepare_sample(L0);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(L.nchunks, L.B);
+  cfg.blockDim = dim3(kSampleThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (L.dl_bf16) return cudaLaunchKernelEx(&cfg, accept_sample_kernel<__nv_bfloat16>, A, L);
+  return cudaLaunchKernelEx(&cfg, accept_sample_kernel<float>, A, L);
+}
+
+cudaError_t launch_sample(const SampleLaunch& L0, cudaStream_t stream) {
+  const SampleLaunch L = prepare_sample(L0);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(L.nchunks, L.B);
   cfg.blockDim = dim3(kSampleThreads);

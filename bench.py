@@ -71,6 +71,9 @@ def parse_args(argv=None):
     ap.add_argument("--loop-c", type=float, default=None,
                     help="time the draft->verify loop with a synthetic drafter costing this "
                          "fraction of a target step per draft token (prints its own line)")
+    ap.add_argument("--vocab-slices", default=None, metavar="G1,G2,...",
+                    help="time one GPU's calls of the vocabulary-parallel step (specdec_shard_*) "
+                         "with W_lm split into G slices, against the single-GPU step")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -263,12 +266,24 @@ def time_oracle(w, inp, mode, budget_s: float, min_steps: int = 1):
     return n / (time.perf_counter() - t0), n
 
 
+# The library's launch plan for a chain step in sampling mode, by the
+# number of (sequence, 4096-token chunk) pairs of the draw: up to 128 the
+# acceptance test and the draw share one kernel; up to 608 the draw is one
+# kernel after the acceptance kernel; beyond, chunk sums and draw are two.
+SAMPLE_CHUNK = 4096
+FUSED_ITEMS = 128
+ONE_DRAW_KERNEL_ITEMS = 608
+
+
 def kernels_per_step(w, mode) -> int:
-    """Library kernels one step launches: LM head, accept, (sample); for a
-    tree, LM head and the tree walk."""
-    if w.tree is not None:
+    """Library kernels one step launches (see the plan above); for a tree,
+    LM head and the tree walk; greedy: LM head and acceptance."""
+    if w.tree is not None or mode != wl.SAMPLE:
         return 2
-    return 3 if mode == wl.SAMPLE else 2
+    items = w.B * -(-w.V // SAMPLE_CHUNK)
+    if items <= FUSED_ITEMS:
+        return 2
+    return 3 if items <= ONE_DRAW_KERNEL_ITEMS else 4
 
 
 # ------------------------------------------------------ multi-rank glue --
@@ -882,6 +897,93 @@ def run_attention(args):
     print(json.dumps(line), flush=True)
 
 
+def run_vocab_slices(args):
+    """One GPU's share of the vocabulary-parallel step ("推测解码", section
+    几段话一起写: the weight read is the cost, so a tensor-parallel target
+    splits W_lm by vocabulary rows). For each G the workload's W_lm is cut
+    into G slices; slice 0's three calls (score, accept, draw) are timed with
+    CUDA events, the exchanges between them done once beforehand from all
+    slices (on G GPUs they are collectives, not timed here: one GPU). L2 is
+    flushed before every timed step; the single-GPU step is timed the same
+    way beside it."""
+    import target_model_verify_gb300 as tv
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = wl.get(args.workload)
+    if w.tree is not None:
+        raise SystemExit("the vocabulary-parallel step runs the chain")
+    mode = wl.SAMPLE if args.mode == "sample" else wl.GREEDY
+    inp = wl.generate(w, args.seed, device=device)
+    B, gamma, d, V, T = w.B, w.gamma, w.d, w.V, w.temperature
+    W, x = inp["W_lm"], inp["draft_tokens"]
+    # read (not written) between steps, so the L2 holds no dirty lines to
+    # write back inside the timed calls
+    flush = torch.ones(128 << 20, dtype=torch.float32, device=device)
+    K, Wm = args.steps, args.warmup
+    peaks, kind = load_peaks()
+
+    def timed_calls(calls):
+        """Median µs of each call over K flushed steps."""
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        times = []
+        for it in range(Wm + K):
+            flush.amax()
+            ev[0].record()
+            for i, fn in enumerate(calls):
+                fn()
+                ev[i + 1].record()
+            torch.cuda.synchronize()
+            if it >= Wm:
+                times.append([ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(len(calls))])
+        return [float(np.median([t[i] for t in times])) for i in range(len(calls))]
+
+    dl_full = inp["draft_logits"] if mode == wl.SAMPLE else None
+    ws = tv.alloc_workspace(B, gamma, d, V, W.dtype, mode, device=device)
+    (single_us,) = timed_calls([lambda: tv.verify(inp["hidden"], W, x, dl_full, T, 1, mode,
+                                                  workspace=ws)])
+    for G in (int(g) for g in args.vocab_slices.split(",")):
+        bounds = [V * g // G for g in range(G + 1)]
+        shards, dls = [], []
+        for g in range(G):
+            v0, v1 = bounds[g], bounds[g + 1]
+            shards.append(tv.VocabShard(W[v0:v1], v0, V, B, gamma, mode, T))
+            dls.append(inp["draft_logits"][:, :, v0:v1].contiguous() if mode == wl.SAMPLE
+                       else None)
+        all_rec = torch.cat([sh.score(inp["hidden"], x, dls[g]).clone()
+                             for g, sh in enumerate(shards)])
+        out = torch.empty(B, gamma + 1, dtype=torch.int32, device=device)
+        nacc = torch.empty(B, dtype=torch.int32, device=device)
+        sums = [sh.accept(all_rec, G, x, dls[g], 1, out, nacc).clone().reshape(-1)
+                for g, sh in enumerate(shards)]
+        all_sums = torch.cat(sums)
+        sh, dl0 = shards[0], dls[0]
+        calls = [lambda: sh.score(inp["hidden"], x, dl0),
+                 lambda: sh.accept(all_rec, G, x, dl0, 1, out, nacc)]
+        if mode == wl.SAMPLE:
+            calls.append(lambda: sh.draw(all_sums, G, 0, dl0, 1, out))
+        us = timed_calls(calls)
+        torch.cuda.synchronize()
+        if tv.read_status(sh.workspace) != 0:
+            raise RuntimeError("device status after the slice's calls")
+        Vs = bounds[1]
+        score_bytes = Vs * d * 2 + B * (gamma + 1) * d * 2 + (B * gamma * Vs * 2 if mode == wl.SAMPLE
+                                                              else 0)
+        gbs = score_bytes / (us[0] * 1e-6) / 1e9
+        print(json.dumps({
+            "metric": "vocabulary-parallel verify step, one GPU's calls (collectives not included)",
+            "slices": G, "V_shard": Vs, "mode": args.mode,
+            "score_us": us[0], "accept_us": us[1], "draw_us": us[2] if len(us) > 2 else 0.0,
+            "slice_calls_us": sum(us), "single_gpu_step_us": single_us,
+            "ideal_slice_us": single_us / G,
+            "score_roofline": {"achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                               "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": score_bytes,
+                               "peak_source": f"{kind} (MEASURED_PEAKS.json)"},
+            "steps": K, "warmup": Wm, "l2": "flushed before every step (512 MB read)",
+            "config": {"workload": args.workload, "B": B, "gamma": gamma, "d": d, "V": V},
+        }), flush=True)
+        del shards, dls, all_rec, sums, all_sums
+
+
 def main(argv=None):
     args = parse_args(argv)
     world, rank, local = dist_env()
@@ -898,6 +1000,9 @@ def main(argv=None):
         return
     if args.gamma_sweep:
         run_gamma_sweep(args)
+        return
+    if args.vocab_slices is not None:
+        run_vocab_slices(args)
         return
     if args.impl == "reference":
         run_reference(args, world, rank, local)

@@ -309,6 +309,66 @@ int specdec_cluster_head(const void* hidden, const void* cluster_emb, const void
                          void* stream);
 
 /*
+ * Vocabulary-parallel verify step, for a tensor-parallel target model whose
+ * LM head is split by vocabulary rows across G GPUs ("推测解码", section
+ * 几段话一起写: the weight read is the step's cost, so each GPU reads only
+ * its slice). GPU g holds rows [v_begin, v_begin + V_shard) of W_lm and the
+ * same columns of every draft row; hidden and draft_tokens are replicated.
+ * The slices must cover [0, V) without overlap. A step is three calls on
+ * every GPU, with the caller's collectives between them (the library holds
+ * no communicator):
+ *
+ *   specdec_shard_score   LM head on the slice; writes this GPU's records
+ *                         (specdec_shard_record_bytes bytes, 16-byte aligned
+ *                         device buffer): per target row (max z, sum exp2,
+ *                         argmax value and global token ID), per draft row
+ *                         (max, sum exp2), per guessed token its two logits
+ *                         when the slice holds it.
+ *   -- all-gather the G records, in rank order, into one device buffer --
+ *   specdec_shard_accept  folds the G records of every row in rank order (so
+ *                         every GPU decides alike), writes out_tokens'
+ *                         kept prefix and n_accepted (greedy mode: the whole
+ *                         result; nothing follows), and in sampling mode the
+ *                         slice's weight sums of the drawn row:
+ *                         shard_sums[2b] = sum of max(0, p - q) (of p for the
+ *                         bonus row), shard_sums[2b+1] = sum of p.
+ *   -- all-gather the G shard_sums [B, 2] fp32, in rank order --
+ *   specdec_shard_draw    every GPU forms the same prefix over slices and
+ *                         t = u * S (S the residual total, or the p total if
+ *                         no residual mass is left); the GPU whose slice
+ *                         holds t writes the drawn token's global ID at
+ *                         out_tokens[b, n_accepted[b]], the others -1.
+ *   -- all-reduce out_tokens with max --
+ *
+ * Same rule, uniforms and token order as specdec_verify(); the draw's
+ * position t is split across slices, so a token can differ from the
+ * single-GPU step's only where u sits within rounding of a CDF boundary.
+ * Every call takes the same shape arguments and the same workspace
+ * (specdec_shard_workspace_size bytes, 256-byte aligned; it carries the
+ * slice's logits and sums from one call to the next). dtype bf16 only;
+ * 1 <= n_shards <= SPECDEC_MAX_SHARDS. Errors as specdec_verify(); a guessed
+ * token that no slice holds sets SPECDEC_ERR_TOKEN_RANGE in the status word
+ * and that sequence's outputs to -1. Asynchronous on `stream`.
+ */
+#define SPECDEC_MAX_SHARDS 64
+size_t specdec_shard_record_bytes(int B, int gamma);
+size_t specdec_shard_workspace_size(int B, int gamma, int d, int V_shard, int mode);
+int specdec_shard_score(const void* hidden, const void* W_shard, const int32_t* draft_tokens,
+                        const void* draft_logits_shard, int B, int gamma, int d, int V_shard,
+                        int v_begin, int V, float temperature, int mode, void* records,
+                        void* workspace, size_t workspace_bytes, void* stream);
+int specdec_shard_accept(const void* all_records, int n_shards, const int32_t* draft_tokens,
+                         const void* draft_logits_shard, int B, int gamma, int d, int V_shard,
+                         int v_begin, int V, float temperature, uint64_t seed, int mode,
+                         int32_t* out_tokens, int32_t* n_accepted, float* shard_sums,
+                         void* workspace, size_t workspace_bytes, void* stream);
+int specdec_shard_draw(const float* all_shard_sums, int n_shards, int shard,
+                       const void* draft_logits_shard, int B, int gamma, int d, int V_shard,
+                       int v_begin, int V, float temperature, uint64_t seed, int mode,
+                       int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                       void* stream);
+
+/*
  * Reads the device status word of a workspace after synchronising `stream`:
  * SPECDEC_OK, SPECDEC_ERR_TIMEOUT, SPECDEC_ERR_TOKEN_RANGE (verify and tree
  * steps) or SPECDEC_ERR_INVALID_ARG (attention lengths, clustered-head

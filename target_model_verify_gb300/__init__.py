@@ -327,6 +327,87 @@ class HostStep:
         return self.out_tokens, self.n_accepted
 
 
+class VocabShard:
+    """One GPU's slice of a vocabulary-parallel LM head (include/specdec_verify.h,
+    specdec_shard_*): rows [v_begin, v_begin + V_shard) of W_lm.
+
+    A step is score() -> all-gather of the records -> accept() -> (sampling)
+    all-gather of the sums -> draw() -> max-reduce of out_tokens;
+    verify_vocab_parallel() runs it with torch.distributed collectives.
+    """
+
+    def __init__(self, W_shard, v_begin, V, B, gamma, mode=SAMPLE, temperature=1.0):
+        if W_shard.dtype != torch.bfloat16 or not W_shard.is_cuda or not W_shard.is_contiguous():
+            raise TypeError("W_shard must be a contiguous bf16 CUDA tensor")
+        self.W, self.v_begin, self.V = W_shard, int(v_begin), int(V)
+        self.V_shard, self.d = W_shard.shape
+        self.B, self.gamma, self.mode, self.T = int(B), int(gamma), int(mode), float(temperature)
+        dev = W_shard.device
+        n = _b.specdec_shard_workspace_size(self.B, self.gamma, self.d, self.V_shard, self.mode)
+        nr = _b.specdec_shard_record_bytes(self.B, self.gamma)
+        if n == 0 or nr == 0:
+            raise SpecdecError(_b.SPECDEC_ERR_UNSUPPORTED, "specdec_shard_workspace_size")
+        self.workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+        self.records = torch.empty(nr, dtype=torch.uint8, device=dev)
+        self.sums = torch.empty(self.B, 2, dtype=torch.float32, device=dev)
+
+    def _shape(self):
+        return (self.B, self.gamma, self.d, self.V_shard, self.v_begin, self.V)
+
+    def score(self, hidden, draft_tokens, draft_logits_shard, stream=None):
+        """LM head on the slice; returns this GPU's records (uint8 device tensor)."""
+        rc = _b.specdec_shard_score(_ptr(hidden), _ptr(self.W), _ptr(draft_tokens),
+                                    _ptr(draft_logits_shard), *self._shape(), self.T, self.mode,
+                                    _ptr(self.records), _ptr(self.workspace),
+                                    self.workspace.numel(), _stream_ptr(stream))
+        _b._check(rc, "specdec_shard_score")
+        return self.records
+
+    def accept(self, all_records, n_shards, draft_tokens, draft_logits_shard, seed, out_tokens,
+               n_accepted, stream=None):
+        """Decides from the gathered records; returns this slice's sums [B, 2]."""
+        rc = _b.specdec_shard_accept(_ptr(all_records), int(n_shards), _ptr(draft_tokens),
+                                     _ptr(draft_logits_shard), *self._shape(), self.T,
+                                     int(seed) & (2 ** 64 - 1), self.mode, _ptr(out_tokens),
+                                     _ptr(n_accepted), _ptr(self.sums), _ptr(self.workspace),
+                                     self.workspace.numel(), _stream_ptr(stream))
+        _b._check(rc, "specdec_shard_accept")
+        return self.sums
+
+    def draw(self, all_sums, n_shards, shard, draft_logits_shard, seed, out_tokens, stream=None):
+        """Writes the drawn token where this slice holds it, -1 elsewhere."""
+        rc = _b.specdec_shard_draw(_ptr(all_sums), int(n_shards), int(shard),
+                                   _ptr(draft_logits_shard), *self._shape(), self.T,
+                                   int(seed) & (2 ** 64 - 1), self.mode, _ptr(out_tokens),
+                                   _ptr(self.workspace), self.workspace.numel(),
+                                   _stream_ptr(stream))
+        _b._check(rc, "specdec_shard_draw")
+
+
+def verify_vocab_parallel(shard, hidden, draft_tokens, draft_logits_shard, seed, group=None):
+    """One vocabulary-parallel verify step on this rank's slice, with the
+    three collectives over `group` (torch.distributed): all-gather of the
+    records, all-gather of the slices' sums, max-reduce of the tokens.
+    Returns (out_tokens [B, gamma+1], n_accepted [B]), identical on every rank."""
+    import torch.distributed as dist
+    G = dist.get_world_size(group)
+    rank = dist.get_rank(group)
+    B, g1 = shard.B, shard.gamma + 1
+    dev = shard.records.device
+    rec = shard.score(hidden, draft_tokens, draft_logits_shard)
+    all_rec = torch.empty(G * rec.numel(), dtype=torch.uint8, device=dev)
+    dist.all_gather_into_tensor(all_rec, rec, group=group)
+    out = torch.empty(B, g1, dtype=torch.int32, device=dev)
+    nacc = torch.empty(B, dtype=torch.int32, device=dev)
+    sums = shard.accept(all_rec, G, draft_tokens, draft_logits_shard, seed, out, nacc)
+    if shard.mode == SAMPLE:
+        all_sums = torch.empty(G * B * 2, dtype=torch.float32, device=dev)
+        dist.all_gather_into_tensor(all_sums, sums.reshape(-1), group=group)
+        shard.draw(all_sums, G, rank, draft_logits_shard, seed, out)
+        dist.all_reduce(out, op=dist.ReduceOp.MAX, group=group)
+    return out, nacc
+
+
 def read_status(workspace, stream=None) -> int:
     """The device status word of the last call that used `workspace`."""
     return _b.specdec_read_status(_ptr(workspace), _stream_ptr(stream))
@@ -344,4 +425,5 @@ def philox_uniforms(seed, B, n_pos, purpose, device="cuda", stream=None):
 __all__ = ["verify", "verify_host", "alloc_workspace", "workspace_bytes", "read_status",
            "philox_uniforms", "status_string", "SpecdecError", "SAMPLE", "GREEDY", "HostStep",
            "verify_tree", "tree_workspace_bytes", "alloc_tree_workspace", "verify_attention",
-           "attention_workspace_bytes", "cluster_head", "ClusterHeadStep"]
+           "attention_workspace_bytes", "cluster_head", "ClusterHeadStep", "VocabShard",
+           "verify_vocab_parallel"]

@@ -59,6 +59,14 @@ _SIGNATURES = {
     "specdec_verify_attention_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
     "specdec_verify_attention": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _vp, _vp,
                                       _sz, _vp]),
+    "specdec_shard_record_bytes": (_sz, [_i, _i]),
+    "specdec_shard_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
+    "specdec_shard_score": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _i, _vp, _vp,
+                                 _sz, _vp]),
+    "specdec_shard_accept": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _u64, _i, _vp,
+                                  _vp, _vp, _vp, _sz, _vp]),
+    "specdec_shard_draw": (_i, [_vp, _i, _i, _vp, _i, _i, _i, _i, _i, _i, _f, _u64, _i, _vp, _vp,
+                                _sz, _vp]),
     "specdec_cluster_head_workspace_size": (_sz, [_i, _i, _i, _i]),
     "specdec_cluster_head": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _f, _u64, _i,
                                   _i, _vp, _vp, _vp, _vp, _sz, _vp]),
@@ -165,6 +173,26 @@ def specdec_cluster_head_workspace_size(M, n_c, top_k, max_cluster) -> int:
 
 def specdec_cluster_head(*args) -> int:
     return int(lib().specdec_cluster_head(*args))
+
+
+def specdec_shard_record_bytes(B, gamma) -> int:
+    return int(lib().specdec_shard_record_bytes(B, gamma))
+
+
+def specdec_shard_workspace_size(B, gamma, d, V_shard, mode) -> int:
+    return int(lib().specdec_shard_workspace_size(B, gamma, d, V_shard, mode))
+
+
+def specdec_shard_score(*args) -> int:
+    return int(lib().specdec_shard_score(*args))
+
+
+def specdec_shard_accept(*args) -> int:
+    return int(lib().specdec_shard_accept(*args))
+
+
+def specdec_shard_draw(*args) -> int:
+    return int(lib().specdec_shard_draw(*args))
 
 
 def specdec_read_status(workspace_ptr: int, stream_ptr: int) -> int:

@@ -45,10 +45,11 @@ __device__ __forceinline__ void accept_fold(const AcceptLaunch& a, int b, Accept
   if (warp == 0 && lane < gamma) {
     const int x = a.draft_tokens[b * gamma + lane];
     sm.x[lane] = x;
-    if (sample && x >= 0 && x < a.V) {
+    const int xl = x - a.tok_offset;   // column of x in this (shard's) vocabulary
+    if (sample && xl >= 0 && xl < a.V) {
       const DL* dl = static_cast<const DL*>(a.dl);
-      sm.zx[lane] = a.z[(size_t)(b * g1 + lane) * a.V + x];
-      sm.zqx[lane] = load_logit(dl, ((size_t)b * gamma + lane) * a.V + x);
+      sm.zx[lane] = a.z[(size_t)(b * g1 + lane) * a.V + xl];
+      sm.zqx[lane] = load_logit(dl, ((size_t)b * gamma + lane) * a.V + xl);
     }
   }
   for (int r = warp; r < rows; r += nwarps) {

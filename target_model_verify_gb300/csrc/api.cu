@@ -317,6 +317,7 @@ int verify_impl(const void* hidden, const void* W, const int32_t* draft_tokens,
   A.p_x = ex.p_x;
   A.q_x = ex.q_x;
   A.argmax_out = ex.argmax_out;
+  A.tok_offset = 0;
   if (!fused && launch_accept(A, stream) != cudaSuccess) return SPECDEC_ERR_CUDA;
 
   if (sample) {
@@ -937,6 +938,215 @@ int specdec_philox_uniforms(uint64_t seed, int B, int n_pos, int purpose, float*
   if (B == 0 || n_pos == 0) return SPECDEC_OK;
   return launch_philox_uniforms(seed, B, n_pos, purpose, out, static_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
+             ? SPECDEC_OK
+             : SPECDEC_ERR_CUDA;
+}
+
+// ------------------------------------------------ vocabulary-parallel --
+
+size_t specdec_shard_record_bytes(int B, int gamma) {
+  if (B < 0 || gamma < 1 || gamma > SPECDEC_MAX_GAMMA) return 0;
+  return shard_record_bytes(B, gamma);
+}
+
+size_t specdec_shard_workspace_size(int B, int gamma, int d, int V_shard, int mode) {
+  if (check_shape(B, gamma, d, V_shard, SPECDEC_BF16, mode) != SPECDEC_OK) return 0;
+  const Plan pl = make_plan(B, gamma, d, V_shard, SPECDEC_BF16, mode);
+  return pl.total + align_up(sizeof(float) * (size_t)B * pl.nchunks);
+}
+
+namespace {
+// Arguments every call of the vocabulary-parallel step shares.
+int shard_check(int B, int gamma, int d, int V_shard, int v_begin, int V, float T, int mode,
+                const void* workspace, size_t workspace_bytes, Plan* pl) {
+  int rc = check_shape(B, gamma, d, V_shard, SPECDEC_BF16, mode);
+  if (rc != SPECDEC_OK) return rc;
+  if (V < 1 || V > kMaxVocab || v_begin < 0 || (long long)v_begin + V_shard > V)
+    return SPECDEC_ERR_UNSUPPORTED;
+  if (mode == SPECDEC_SAMPLE && (!(T > 0.f) || !std::isfinite(T))) return SPECDEC_ERR_INVALID_ARG;
+  *pl = make_plan(B, gamma, d, V_shard, SPECDEC_BF16, mode);
+  const size_t need = pl->total + align_up(sizeof(float) * (size_t)B * pl->nchunks);
+  if (!workspace || ((uintptr_t)workspace % kAlign) != 0 || workspace_bytes < need)
+    return SPECDEC_ERR_WORKSPACE;
+  return SPECDEC_OK;
+}
+
+SampleLaunch shard_sample_launch(const Plan& pl, char* ws, const void* dl_shard, int B, int gamma,
+                                 int V_shard, float T, uint64_t seed, int32_t* out_tokens) {
+  SampleLaunch S;
+  S.B = B;
+  S.gamma = gamma;
+  S.V = V_shard;
+  S.nchunks = pl.nchunks;
+  S.dl_bf16 = 1;
+  S.vec = 0;
+  S.prefetch = 0;
+  S.c = kLog2e / T;
+  S.seed = seed;
+  S.z = reinterpret_cast<float*>(ws + pl.off_z);
+  S.dl = dl_shard;
+  S.sel = reinterpret_cast<SelectedRow*>(ws + pl.off_sel);
+  S.chunk_sums = reinterpret_cast<float*>(ws + pl.off_chunks);
+  S.counters = reinterpret_cast<int*>(ws + pl.off_counters);
+  S.out_tokens = out_tokens;
+  return S;
+}
+}  // namespace
+
+int specdec_shard_score(const void* hidden, const void* W_shard, const int32_t* draft_tokens,
+                        const void* draft_logits_shard, int B, int gamma, int d, int V_shard,
+                        int v_begin, int V, float temperature, int mode, void* records,
+                        void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  Plan pl;
+  int rc = shard_check(B, gamma, d, V_shard, v_begin, V, temperature, mode, workspace,
+                       workspace_bytes, &pl);
+  if (rc != SPECDEC_OK) return rc;
+  if (B == 0) return SPECDEC_OK;
+  const bool sample = mode == SPECDEC_SAMPLE;
+  if (!hidden || !W_shard || !draft_tokens || !records || (sample && !draft_logits_shard))
+    return SPECDEC_ERR_INVALID_ARG;
+  if ((((uintptr_t)hidden | (uintptr_t)W_shard) & 15u) != 0 || ((uintptr_t)records & 15u) != 0)
+    return SPECDEC_ERR_INVALID_ARG;
+  const int nsm = num_sms_current();
+  if (nsm <= 0) return SPECDEC_ERR_CUDA;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  PartialP* pp = reinterpret_cast<PartialP*>(ws + pl.off_pp);
+  PartialQ* pq = reinterpret_cast<PartialQ*>(ws + pl.off_pq);
+  float* z = sample ? reinterpret_cast<float*>(ws + pl.off_z) : nullptr;
+  const float c = sample ? kLog2e / temperature : kLog2e;
+  EpiParams ep;
+  ep.M = pl.M;
+  ep.V = V_shard;
+  ep.gamma = gamma;
+  ep.P = 0;
+  ep.c = c;
+  ep.sample = sample ? 1 : 0;
+  ep.want_argmax = sample ? 0 : 1;
+  ep.zout = z;
+  ep.dl = draft_logits_shard;
+  ep.pp = pp;
+  ep.pq = pq;
+  ep.run = nullptr;
+  ep.q_in_epilogue = 1;
+  const bool q_stream = sample && B * gamma > kQWarpMaxRows;
+  ep.q_warps = q_stream ? 0 : 1;
+  ep.q_stream = q_stream ? 1 : 0;
+  ep.n_qrows = B * gamma;
+  const int Pq = q_stream ? (V_shard + kQChunk - 1) / kQChunk : 0;
+  ep.Pq = Pq;
+  ep.q_vec = (V_shard % 8 == 0 && ((uintptr_t)draft_logits_shard & 15u) == 0) ? 1 : 0;
+  ep.counters = nullptr;
+  ep.n_counters = 0;
+  int P = 0;
+  rc = lmhead_stage_bf16(hidden, W_shard, pl.M, d, V_shard, ep, status, ws, pl.off_tickets,
+                         pl.off_fix, next_call_epoch(), nsm, stream, &P);
+  if (rc != SPECDEC_OK) return rc;
+  AcceptLaunch A;
+  A.B = B;
+  A.gamma = gamma;
+  A.V = V_shard;
+  A.P = P;
+  A.Pq = q_stream ? Pq : P;
+  A.mode = mode;
+  A.dl_bf16 = 1;
+  A.c = c;
+  A.seed = 0;
+  A.pp = pp;
+  A.pq = pq;
+  A.z = z;
+  A.dl = draft_logits_shard;
+  A.draft_tokens = draft_tokens;
+  A.out_tokens = nullptr;
+  A.n_accepted = nullptr;
+  A.sel = nullptr;
+  A.counters = nullptr;
+  A.status = status;
+  A.calls = header_calls(status);
+  A.lse_p = A.lse_q = A.p_x = A.q_x = nullptr;
+  A.argmax_out = nullptr;
+  A.tok_offset = v_begin;
+  return launch_shard_fold(A, records, stream) == cudaSuccess ? SPECDEC_OK : SPECDEC_ERR_CUDA;
+}
+
+int specdec_shard_accept(const void* all_records, int n_shards, const int32_t* draft_tokens,
+                         const void* draft_logits_shard, int B, int gamma, int d, int V_shard,
+                         int v_begin, int V, float temperature, uint64_t seed, int mode,
+                         int32_t* out_tokens, int32_t* n_accepted, float* shard_sums,
+                         void* workspace, size_t workspace_bytes, void* stream_ptr) {
+  Plan pl;
+  int rc = shard_check(B, gamma, d, V_shard, v_begin, V, temperature, mode, workspace,
+                       workspace_bytes, &pl);
+  if (rc != SPECDEC_OK) return rc;
+  if (B == 0) return SPECDEC_OK;
+  const bool sample = mode == SPECDEC_SAMPLE;
+  if (!all_records || n_shards < 1 || n_shards > SPECDEC_MAX_SHARDS || !draft_tokens ||
+      !out_tokens || !n_accepted || (sample && (!draft_logits_shard || !shard_sums)))
+    return SPECDEC_ERR_INVALID_ARG;
+  if (((uintptr_t)all_records & 15u) != 0 || ((uintptr_t)shard_sums & 7u) != 0)
+    return SPECDEC_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  int* status = reinterpret_cast<int*>(ws);
+  const float c = sample ? kLog2e / temperature : kLog2e;
+  AcceptLaunch A;
+  A.B = B;
+  A.gamma = gamma;
+  A.V = V;
+  A.P = 0;
+  A.Pq = 0;
+  A.mode = mode;
+  A.dl_bf16 = 1;
+  A.c = c;
+  A.seed = seed;
+  A.pp = nullptr;
+  A.pq = nullptr;
+  A.z = nullptr;
+  A.dl = nullptr;
+  A.draft_tokens = draft_tokens;
+  A.out_tokens = out_tokens;
+  A.n_accepted = n_accepted;
+  A.sel = reinterpret_cast<SelectedRow*>(ws + pl.off_sel);
+  A.counters = reinterpret_cast<int*>(ws + pl.off_counters);
+  A.status = status;
+  A.calls = header_calls(status);
+  A.lse_p = A.lse_q = A.p_x = A.q_x = nullptr;
+  A.argmax_out = nullptr;
+  A.tok_offset = 0;
+  if (launch_shard_accept(A, all_records, shard_record_bytes(B, gamma), n_shards, stream) !=
+      cudaSuccess)
+    return SPECDEC_ERR_CUDA;
+  if (!sample) return SPECDEC_OK;
+  const SampleLaunch S = shard_sample_launch(pl, ws, draft_logits_shard, B, gamma, V_shard,
+                                             temperature, seed, out_tokens);
+  float* cs_p = reinterpret_cast<float*>(ws + pl.total);
+  return launch_shard_sums(S, cs_p, reinterpret_cast<float2*>(shard_sums), stream) == cudaSuccess
+             ? SPECDEC_OK
+             : SPECDEC_ERR_CUDA;
+}
+
+int specdec_shard_draw(const float* all_shard_sums, int n_shards, int shard,
+                       const void* draft_logits_shard, int B, int gamma, int d, int V_shard,
+                       int v_begin, int V, float temperature, uint64_t seed, int mode,
+                       int32_t* out_tokens, void* workspace, size_t workspace_bytes,
+                       void* stream_ptr) {
+  Plan pl;
+  int rc = shard_check(B, gamma, d, V_shard, v_begin, V, temperature, mode, workspace,
+                       workspace_bytes, &pl);
+  if (rc != SPECDEC_OK) return rc;
+  if (B == 0 || mode == SPECDEC_GREEDY) return SPECDEC_OK;
+  if (!all_shard_sums || n_shards < 1 || n_shards > SPECDEC_MAX_SHARDS || shard < 0 ||
+      shard >= n_shards || !draft_logits_shard || !out_tokens ||
+      ((uintptr_t)all_shard_sums & 7u) != 0)
+    return SPECDEC_ERR_INVALID_ARG;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+  char* ws = static_cast<char*>(workspace);
+  const SampleLaunch S = shard_sample_launch(pl, ws, draft_logits_shard, B, gamma, V_shard,
+                                             temperature, seed, out_tokens);
+  const float* cs_p = reinterpret_cast<const float*>(ws + pl.total);
+  return launch_shard_draw(S, cs_p, reinterpret_cast<const float2*>(all_shard_sums), n_shards,
+                           shard, v_begin, stream) == cudaSuccess
              ? SPECDEC_OK
              : SPECDEC_ERR_CUDA;
 }

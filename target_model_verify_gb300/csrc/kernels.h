@@ -56,6 +56,7 @@ struct AcceptLaunch {
   float* p_x;
   float* q_x;
   int32_t* argmax_out;
+  int tok_offset;                // vocabulary-parallel shard: first token ID it holds (else 0)
 };
 cudaError_t launch_accept(const AcceptLaunch& L, cudaStream_t stream);
 
@@ -86,6 +87,35 @@ constexpr long long kFusedAcceptItems = 128;
 bool fused_accept_sample(int B, int nchunks);
 cudaError_t launch_accept_sample(const AcceptLaunch& A, const SampleLaunch& L,
                                  cudaStream_t stream);
+
+// Vocabulary-parallel step (one slice of the vocabulary per GPU). A slice's
+// records: target rows [M] (max z, sum exp2, argmax value and global token
+// ID), draft rows [B*gamma] (max, sum exp2), guessed tokens [B*gamma] (the
+// two logits when this slice holds the token); segments 256-byte aligned.
+struct ShardRec {
+  float m, s, amax_v;
+  int amax_i;
+};
+struct ShardQRec {
+  float m, s;
+};
+struct ShardXRec {
+  float zx, zqx;
+  int owned, pad;
+};
+size_t shard_record_bytes(int B, int gamma);
+// Fold the slice's LM-head records into one record per row (A.V = the
+// slice's vocabulary, A.tok_offset = its first token ID).
+cudaError_t launch_shard_fold(const AcceptLaunch& A, void* records, cudaStream_t stream);
+// Fold the gathered records of all slices and decide (A.V = the whole vocabulary).
+cudaError_t launch_shard_accept(const AcceptLaunch& A, const void* all_records,
+                                size_t record_bytes, int n_shards, cudaStream_t stream);
+// The slice's (residual, p) weight sums of each sequence's drawn row.
+cudaError_t launch_shard_sums(const SampleLaunch& L, float* cs_p, float2* shard_sums,
+                              cudaStream_t stream);
+// The draw: the slice holding t = u * S writes its token, the others -1.
+cudaError_t launch_shard_draw(const SampleLaunch& L, const float* cs_p, const float2* all_sums,
+                              int n_shards, int shard, int tok_offset, cudaStream_t stream);
 
 // Tree verification walk: one cluster of kTreeCluster CTAs per sequence
 // (sampling; the CTAs split the vocabulary), kTreeClusterWide when every

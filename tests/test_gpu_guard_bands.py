@@ -248,3 +248,55 @@ def test_host_entry_point_stays_inside_its_buffers(mode, pinned):
     dev_out, dev_nacc, _ = parity.run_library(inp, 1.0, 5, mode, debug=False)
     np.testing.assert_array_equal(out.numpy(), dev_out)
     np.testing.assert_array_equal(nacc.numpy(), dev_nacc)
+
+
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+@pytest.mark.parametrize("B,gamma,d,V,bounds", [
+    pytest.param(4, 4, 256, 3001, (0, 1000, 3001), id="two_slices_ragged"),
+    pytest.param(64, 3, 128, 3000, (0, 1499, 3000), id="row_owner_slices_ragged"),
+    pytest.param(8, 4, 4096, 128256, (0, 32064, 64128, 96192, 128256), id="llama_four_slices"),
+])
+def test_vocab_parallel_calls_stay_inside_their_buffers(B, gamma, d, V, bounds, mode):
+    """specdec_shard_score / _accept / _draw: every slice's workspace,
+    records, sums and outputs guarded, the exchanges done in between."""
+    import target_model_verify_gb300 as tv
+    from target_model_verify_gb300 import _binding as b
+    w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, sigma=0.5)
+    inp = wl.generate(w, 8, device=DEV)
+    G = len(bounds) - 1
+    shards, guards, dls = [], [], []
+    for g in range(G):
+        v0, v1 = bounds[g], bounds[g + 1]
+        sh = tv.VocabShard(inp["W_lm"][v0:v1].contiguous(), v0, V, B, gamma, mode, 1.0)
+        gw = Guarded(sh.workspace.numel())
+        gr = Guarded(b.specdec_shard_record_bytes(B, gamma))
+        gs = Guarded(B * 8)
+        sh.workspace, sh.records, sh.sums = gw.body, gr.body, gs.typed(torch.float32, (B, 2))
+        shards.append(sh)
+        guards.append((gw, gr, gs))
+        dls.append(inp["draft_logits"][:, :, v0:v1].contiguous() if mode == ov.SAMPLE else None)
+    recs = torch.cat([sh.score(inp["hidden"], inp["draft_tokens"], dls[g]).clone()
+                      for g, sh in enumerate(shards)])
+    outs = [_out_buffers(B, gamma + 1) for _ in range(G)]
+    sums = []
+    for g, sh in enumerate(shards):
+        o, n = outs[g]
+        s = sh.accept(recs, G, inp["draft_tokens"], dls[g], 5,
+                      o.typed(torch.int32, (B, gamma + 1)), n.typed(torch.int32, (B,)))
+        sums.append(s.clone().reshape(-1))
+    if mode == ov.SAMPLE:
+        all_sums = torch.cat(sums)
+        for g, sh in enumerate(shards):
+            sh.draw(all_sums, G, g, dls[g], 5, outs[g][0].typed(torch.int32, (B, gamma + 1)))
+    torch.cuda.synchronize()
+    for g, (gw, gr, gs) in enumerate(guards):
+        assert tv.read_status(gw.body) == 0
+        gw.check(f"workspace of slice {g}")
+        gr.check(f"records of slice {g}")
+        gs.check(f"sums of slice {g}")
+        outs[g][0].check(f"out_tokens of slice {g}")
+        outs[g][1].check(f"n_accepted of slice {g}")
+    out = torch.stack([o.typed(torch.int32, (B, gamma + 1)) for o, _ in outs]).amax(dim=0)
+    nacc = outs[0][1].typed(torch.int32, (B,))
+    parity.check_structure(out.cpu().numpy(), nacc.cpu().numpy(),
+                           inp["draft_tokens"].cpu().numpy(), V)

@@ -1,0 +1,132 @@
+"""The vocabulary-parallel verify step (specdec_shard_*) on one GPU.
+
+Each test splits W_lm and the draft logits into G vocabulary slices and
+runs every slice's three calls on cuda:0 in turn, standing in for the G
+GPUs of a tensor-parallel LM head: the all-gathers are concatenations in
+rank order and the final max-reduce an elementwise max, which is what the
+collectives of verify_vocab_parallel() compute. No slice's kernels wait on
+another's (the exchange happens between calls), so running them one after
+another on one GPU is the same computation.
+
+Results are checked against the fp64 oracle on the whole vocabulary under
+the parity rule of the single-GPU step (tests/parity.py), and against the
+single-GPU step itself: tokens and counts must agree except where the
+oracle's margin is below the rule's threshold (the draw's position is
+split across slices in a different order of additions).
+"""
+import numpy as np
+import pytest
+import torch
+
+from oracle import verify as ov
+from target_model_verify_gb300 import workloads as wl
+
+from . import parity
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    from target_model_verify_gb300 import build
+    build.build()
+    import target_model_verify_gb300  # noqa: F401  (fails loudly if the library is missing)
+    torch.cuda.init()
+
+
+def _run_sharded(inp, bounds, T, seed, mode):
+    """All slices' calls, the exchanges emulated in rank order."""
+    import target_model_verify_gb300 as tv
+    W, dl = inp["W_lm"], inp["draft_logits"]
+    B, g1, _ = inp["hidden"].shape
+    V = W.shape[0]
+    G = len(bounds) - 1
+    shards, dls = [], []
+    for g in range(G):
+        v0, v1 = bounds[g], bounds[g + 1]
+        shards.append(tv.VocabShard(W[v0:v1].contiguous(), v0, V, B, g1 - 1, mode, T))
+        dls.append(dl[:, :, v0:v1].contiguous() if mode == ov.SAMPLE else None)
+    recs = [sh.score(inp["hidden"], inp["draft_tokens"], dls[g]).clone()
+            for g, sh in enumerate(shards)]
+    all_rec = torch.cat(recs)
+    outs, naccs, sums = [], [], []
+    for g, sh in enumerate(shards):
+        out = torch.full((B, g1), -7, dtype=torch.int32, device=DEV)
+        nacc = torch.full((B,), -7, dtype=torch.int32, device=DEV)
+        s = sh.accept(all_rec, G, inp["draft_tokens"], dls[g], seed, out, nacc)
+        outs.append(out)
+        naccs.append(nacc)
+        sums.append(s.clone())
+    if mode == ov.SAMPLE:
+        all_sums = torch.cat([s.reshape(-1) for s in sums])
+        for g, sh in enumerate(shards):
+            sh.draw(all_sums, G, g, dls[g], seed, outs[g])
+    torch.cuda.synchronize()
+    for sh in shards:
+        assert tv.read_status(sh.workspace) == 0
+    # every slice decided alike: same kept prefix and counts everywhere
+    for g in range(1, G):
+        assert torch.equal(naccs[g], naccs[0])
+    out = torch.stack(outs).amax(dim=0)
+    if mode == ov.SAMPLE:
+        # exactly one slice drew each sequence's token
+        nacc = naccs[0].long()
+        drawn = torch.stack([o.gather(1, nacc[:, None])[:, 0] for o in outs])
+        assert torch.all((drawn >= 0).sum(dim=0) == 1)
+    return out.cpu().numpy(), naccs[0].cpu().numpy()
+
+
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+@pytest.mark.parametrize("B,gamma,d,V,bounds", [
+    (4, 4, 256, 3001, (0, 1000, 2100, 3001)),          # three uneven slices, ragged tails
+    (2, 1, 64, 128, (0, 128)),                         # one slice: the single-GPU step
+    (16, 4, 128, 2049, (0, 640, 1281, 1900, 2049)),    # four slices, pairs with stream-K
+    (64, 3, 128, 3000, (0, 1501, 3000)),               # row-owner tiles on each slice
+])
+def test_sharded_step_matches_the_oracle(B, gamma, d, V, bounds, mode):
+    w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, temperature=0.9, sigma=0.5)
+    inp = wl.generate(w, 17 + B, device=DEV)
+    out, nacc = _run_sharded(inp, bounds, w.temperature, 5, mode)
+    res = parity.run_oracle(inp, w.temperature, 5, mode)
+    parity.assert_tokens(out, nacc, res, mode)
+    parity.check_structure(out, nacc, inp["draft_tokens"].cpu().numpy(), V)
+    ref_out, ref_nacc, _ = parity.run_library(inp, w.temperature, 5, mode, debug=False)
+    diff = np.nonzero((out != ref_out).any(axis=1) | (nacc != ref_nacc))[0]
+    for b in diff:   # only where the oracle itself sat on a boundary
+        m = parity.first_difference_margin(res, int(b), out[b], int(nacc[b]), mode)
+        assert m < (parity.GREEDY_GAP if mode == ov.GREEDY else parity.SAMPLE_MARGIN), (b, m)
+
+
+@pytest.mark.parametrize("mode", [ov.SAMPLE, ov.GREEDY])
+def test_sharded_llama_head_four_slices(mode):
+    """The Llama-3-8B-shaped head split over four GPUs' worth of slices,
+    eight sequences, every sequence against the fp64 oracle."""
+    w = wl.get("llama3_8b_head", B=8)
+    inp = wl.generate(w, 9, device=DEV)
+    V = w.V
+    bounds = tuple(V * g // 4 for g in range(5))
+    out, nacc = _run_sharded(inp, bounds, w.temperature, 3, mode)
+    res = parity.run_oracle(inp, w.temperature, 3, mode)
+    parity.assert_tokens(out, nacc, res, mode)
+    parity.check_structure(out, nacc, inp["draft_tokens"].cpu().numpy(), V)
+
+
+def test_sharded_token_out_of_range_sets_status():
+    import target_model_verify_gb300 as tv
+    w = wl.get("llama3_8b_head", B=3, gamma=4, d=128, V=1000, sigma=0.5)
+    inp = wl.generate(w, 4, device=DEV)
+    bad = dict(inp, draft_tokens=inp["draft_tokens"].clone())
+    bad["draft_tokens"][1, 0] = w.V + 5
+    bounds = (0, 500, 1000)
+    shards = [tv.VocabShard(inp["W_lm"][a:b].contiguous(), a, w.V, w.B, w.gamma, ov.SAMPLE, 1.0)
+              for a, b in zip(bounds[:-1], bounds[1:])]
+    dls = [inp["draft_logits"][:, :, a:b].contiguous() for a, b in zip(bounds[:-1], bounds[1:])]
+    all_rec = torch.cat([sh.score(bad["hidden"], bad["draft_tokens"], dls[g]).clone()
+                         for g, sh in enumerate(shards)])
+    out = torch.empty(w.B, w.gamma + 1, dtype=torch.int32, device=DEV)
+    nacc = torch.empty(w.B, dtype=torch.int32, device=DEV)
+    shards[0].accept(all_rec, 2, bad["draft_tokens"], dls[0], 1, out, nacc)
+    assert tv.read_status(shards[0].workspace) == tv._b.SPECDEC_ERR_TOKEN_RANGE
+    assert int(nacc[1]) == -1 and bool((out[1] == -1).all())
+    assert int(nacc[0]) >= 0 and int(nacc[2]) >= 0

@@ -902,10 +902,11 @@ def run_vocab_slices(args):
     几段话一起写: the weight read is the cost, so a tensor-parallel target
     splits W_lm by vocabulary rows). For each G the workload's W_lm is cut
     into G slices; slice 0's three calls (score, accept, draw) are timed with
-    CUDA events, the exchanges between them done once beforehand from all
-    slices (on G GPUs they are collectives, not timed here: one GPU). L2 is
-    flushed before every timed step; the single-GPU step is timed the same
-    way beside it."""
+    CUDA events, each alone and the three back to back (slice_calls_us),
+    the exchanges between them done once beforehand from all slices (on G
+    GPUs they are collectives, not timed here: one GPU). L2 is flushed (by a
+    512 MB read) before every timed step; the single-GPU step is timed the
+    same way beside it."""
     import target_model_verify_gb300 as tv
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
@@ -923,7 +924,10 @@ def run_vocab_slices(args):
     peaks, kind = load_peaks()
 
     def timed_calls(calls):
-        """Median µs of each call over K flushed steps."""
+        """Mean µs of each call (events between the calls) and of the calls
+        back to back (events around them only), over K flushed steps each.
+        Means, not medians: the event clock ticks in ~2 µs steps here, and
+        the mean of many ticks is unbiased where the median is not."""
         ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
         times = []
         for it in range(Wm + K):
@@ -935,12 +939,23 @@ def run_vocab_slices(args):
             torch.cuda.synchronize()
             if it >= Wm:
                 times.append([ev[i].elapsed_time(ev[i + 1]) * 1e3 for i in range(len(calls))])
-        return [float(np.median([t[i] for t in times])) for i in range(len(calls))]
+        whole = []
+        for it in range(Wm + K):
+            flush.amax()
+            ev[0].record()
+            for fn in calls:
+                fn()
+            ev[1].record()
+            torch.cuda.synchronize()
+            if it >= Wm:
+                whole.append(ev[0].elapsed_time(ev[1]) * 1e3)
+        return [float(np.mean([t[i] for t in times])) for i in range(len(calls))], \
+            float(np.mean(whole))
 
     dl_full = inp["draft_logits"] if mode == wl.SAMPLE else None
     ws = tv.alloc_workspace(B, gamma, d, V, W.dtype, mode, device=device)
-    (single_us,) = timed_calls([lambda: tv.verify(inp["hidden"], W, x, dl_full, T, 1, mode,
-                                                  workspace=ws)])
+    _, single_us = timed_calls([lambda: tv.verify(inp["hidden"], W, x, dl_full, T, 1, mode,
+                                                 workspace=ws)])
     for G in (int(g) for g in args.vocab_slices.split(",")):
         bounds = [V * g // G for g in range(G + 1)]
         shards, dls = [], []
@@ -961,7 +976,7 @@ def run_vocab_slices(args):
                  lambda: sh.accept(all_rec, G, x, dl0, 1, out, nacc)]
         if mode == wl.SAMPLE:
             calls.append(lambda: sh.draw(all_sums, G, 0, dl0, 1, out))
-        us = timed_calls(calls)
+        us, whole_us = timed_calls(calls)
         torch.cuda.synchronize()
         if tv.read_status(sh.workspace) != 0:
             raise RuntimeError("device status after the slice's calls")
@@ -973,7 +988,7 @@ def run_vocab_slices(args):
             "metric": "vocabulary-parallel verify step, one GPU's calls (collectives not included)",
             "slices": G, "V_shard": Vs, "mode": args.mode,
             "score_us": us[0], "accept_us": us[1], "draw_us": us[2] if len(us) > 2 else 0.0,
-            "slice_calls_us": sum(us), "single_gpu_step_us": single_us,
+            "slice_calls_us": whole_us, "single_gpu_step_us": single_us,
             "ideal_slice_us": single_us / G,
             "score_roofline": {"achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                                "frac": gbs / peaks["hbm_gbs"], "algorithmic_bytes": score_bytes,

@@ -325,8 +325,8 @@ int specdec_cluster_head(const void* hidden, const void* cluster_emb, const void
  *                         (max, sum exp2), per guessed token its two logits
  *                         when the slice holds it.
  *   -- all-gather the G records, in rank order, into one device buffer --
- *   specdec_shard_accept  folds the G records of every row in rank order (so
- *                         every GPU decides alike), writes out_tokens'
+ *   specdec_shard_accept  folds the G records of every row in one fixed
+ *                         order (so every GPU decides alike), writes out_tokens'
  *                         kept prefix and n_accepted (greedy mode: the whole
  *                         result; nothing follows), and in sampling mode the
  *                         slice's weight sums of the drawn row:
@@ -345,7 +345,9 @@ int specdec_cluster_head(const void* hidden, const void* cluster_emb, const void
  * single-GPU step's only where u sits within rounding of a CDF boundary.
  * Every call takes the same shape arguments and the same workspace
  * (specdec_shard_workspace_size bytes, 256-byte aligned; it carries the
- * slice's logits and sums from one call to the next). dtype bf16 only;
+ * slice's logits and sums from one call to the next, and the score call
+ * resets the counters the accept call uses, so each accept follows the
+ * score of its own step on that workspace). dtype bf16 only;
  * 1 <= n_shards <= SPECDEC_MAX_SHARDS. Errors as specdec_verify(); a guessed
  * token that no slice holds sets SPECDEC_ERR_TOKEN_RANGE in the status word
  * and that sequence's outputs to -1. Asynchronous on `stream`.

@@ -1037,8 +1037,9 @@ int specdec_shard_score(const void* hidden, const void* W_shard, const int32_t* 
   const int Pq = q_stream ? (V_shard + kQChunk - 1) / kQChunk : 0;
   ep.Pq = Pq;
   ep.q_vec = (V_shard % 8 == 0 && ((uintptr_t)draft_logits_shard & 15u) == 0) ? 1 : 0;
-  ep.counters = nullptr;
-  ep.n_counters = 0;
+  // the chunk tickets of the fused accept-and-sums kernel
+  ep.counters = sample ? reinterpret_cast<int*>(ws + pl.off_counters) : nullptr;
+  ep.n_counters = sample ? B : 0;
   int P = 0;
   rc = lmhead_stage_bf16(hidden, W_shard, pl.M, d, V_shard, ep, status, ws, pl.off_tickets,
                          pl.off_fix, next_call_epoch(), nsm, stream, &P);
@@ -1114,13 +1115,21 @@ int specdec_shard_accept(const void* all_records, int n_shards, const int32_t* d
   A.lse_p = A.lse_q = A.p_x = A.q_x = nullptr;
   A.argmax_out = nullptr;
   A.tok_offset = 0;
-  if (launch_shard_accept(A, all_records, shard_record_bytes(B, gamma), n_shards, stream) !=
-      cudaSuccess)
+  const size_t rb = shard_record_bytes(B, gamma);
+  float* cs_p = reinterpret_cast<float*>(ws + pl.total);
+  if (sample && shard_fused_accept_sums(B, pl.nchunks)) {
+    const SampleLaunch S = shard_sample_launch(pl, ws, draft_logits_shard, B, gamma, V_shard,
+                                               temperature, seed, out_tokens);
+    return launch_shard_accept_sums(A, S, all_records, rb, n_shards, cs_p,
+                                    reinterpret_cast<float2*>(shard_sums), stream) == cudaSuccess
+               ? SPECDEC_OK
+               : SPECDEC_ERR_CUDA;
+  }
+  if (launch_shard_accept(A, all_records, rb, n_shards, stream) != cudaSuccess)
     return SPECDEC_ERR_CUDA;
   if (!sample) return SPECDEC_OK;
   const SampleLaunch S = shard_sample_launch(pl, ws, draft_logits_shard, B, gamma, V_shard,
                                              temperature, seed, out_tokens);
-  float* cs_p = reinterpret_cast<float*>(ws + pl.total);
   return launch_shard_sums(S, cs_p, reinterpret_cast<float2*>(shard_sums), stream) == cudaSuccess
              ? SPECDEC_OK
              : SPECDEC_ERR_CUDA;

@@ -111,6 +111,12 @@ cudaError_t launch_shard_fold(const AcceptLaunch& A, void* records, cudaStream_t
 cudaError_t launch_shard_accept(const AcceptLaunch& A, const void* all_records,
                                 size_t record_bytes, int n_shards, cudaStream_t stream);
 // The slice's (residual, p) weight sums of each sequence's drawn row.
+// Few sequences (B * chunks <= kFusedAcceptItems): accept and the slice sums
+// in one kernel; its chunk tickets use counters the LM head zeroed.
+bool shard_fused_accept_sums(int B, int nchunks);
+cudaError_t launch_shard_accept_sums(const AcceptLaunch& A, const SampleLaunch& L,
+                                     const void* all_records, size_t record_bytes, int n_shards,
+                                     float* cs_p, float2* shard_sums, cudaStream_t stream);
 cudaError_t launch_shard_sums(const SampleLaunch& L, float* cs_p, float2* shard_sums,
                               cudaStream_t stream);
 // The draw: the slice holding t = u * S writes its token, the others -1.

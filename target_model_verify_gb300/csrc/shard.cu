@@ -34,6 +34,7 @@ using namespace sampling;
 
 constexpr int kFoldThreads = 512;
 constexpr int kAccThreads = 256;
+static_assert(kAccThreads == kSampleThreads, "the fused kernel sums chunks with the sampler's layout");
 
 __host__ __device__ inline size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -83,23 +84,19 @@ __global__ void __launch_bounds__(kFoldThreads) shard_fold_kernel(const AcceptLa
   }
 }
 
-// One CTA per sequence: fold the G slices' records in rank order, then the
-// acceptance decision of the single-GPU step (accept_decide) on the folded
-// values.
+// Folds the G slices' records of sequence b in a fixed order (identical on
+// every GPU), looks up the slice holding each guessed token, and takes the
+// acceptance decision of the single-GPU step (accept_decide, warp 0) on the
+// folded values; `outputs` writes the kept prefix, n_accepted and the
+// status. All threads of the CTA (kAccThreads) enter.
 template <typename DL>
-__global__ void __launch_bounds__(kAccThreads) shard_accept_kernel(const AcceptLaunch a,
-                                                                   const void* all_records,
-                                                                   size_t record_bytes,
-                                                                   int n_shards) {
-  __shared__ AcceptSmem sm;
-  __shared__ int s_noowner;
-  const int b = blockIdx.x;
+__device__ __forceinline__ void shard_fold_decide(const AcceptLaunch& a, int b, AcceptSmem& sm,
+                                                  const char* base, size_t record_bytes,
+                                                  int n_shards, bool outputs) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gamma = a.gamma, g1 = gamma + 1;
   const bool sample = a.mode == SPECDEC_SAMPLE;
-  const char* base = static_cast<const char*>(all_records);
-  grid_dependency_wait();
-  if (threadIdx.x == 0) s_noowner = 0;
+  const int B = a.B;
   const int rows = g1 + (sample ? gamma : 0);
   for (int r = warp; r < rows; r += kAccThreads / 32) {
     float m = -INFINITY, s = 0.f, av = -INFINITY;
@@ -107,8 +104,7 @@ __global__ void __launch_bounds__(kAccThreads) shard_accept_kernel(const AcceptL
     // lanes take shards lane, lane+32, ...; the warp merge then visits them
     // in a fixed order, identical on every GPU.
     for (int k = lane; k < n_shards; k += 32) {
-      const ShardPtrs rp = shard_ptrs(const_cast<char*>(base) + (size_t)k * record_bytes, gridDim.x,
-                                      gamma);
+      const ShardPtrs rp = shard_ptrs(const_cast<char*>(base) + (size_t)k * record_bytes, B, gamma);
       if (r < g1) {
         const ShardRec x = rp.P[b * g1 + r];
         softmax_merge(m, s, x.m, x.s, a.c);
@@ -146,8 +142,7 @@ __global__ void __launch_bounds__(kAccThreads) shard_accept_kernel(const AcceptL
     int own = -1;
     float zx = 0.f, zqx = 0.f;
     for (int k = 0; k < n_shards && own < 0; ++k) {
-      const ShardPtrs rp = shard_ptrs(const_cast<char*>(base) + (size_t)k * record_bytes, gridDim.x,
-                                      gamma);
+      const ShardPtrs rp = shard_ptrs(const_cast<char*>(base) + (size_t)k * record_bytes, B, gamma);
       const ShardXRec xr = rp.X[b * gamma + lane];
       if (xr.owned) {
         own = k;
@@ -161,12 +156,74 @@ __global__ void __launch_bounds__(kAccThreads) shard_accept_kernel(const AcceptL
     sm.zqx[lane] = zqx;
   }
   __syncthreads();
-  if (threadIdx.x >= 32) return;
-  accept_decide<DL>(a, b, sm, true);
-  if (threadIdx.x == 0 && sample) {
+  if (warp == 0) accept_decide<DL>(a, b, sm, outputs);
+  __syncthreads();
+}
+
+// One CTA per sequence: the decision (shard_fold_decide) and the selected
+// row for the sums kernel.
+template <typename DL>
+__global__ void __launch_bounds__(kAccThreads) shard_accept_kernel(const AcceptLaunch a,
+                                                                   const void* all_records,
+                                                                   size_t record_bytes,
+                                                                   int n_shards) {
+  __shared__ AcceptSmem sm;
+  const int b = blockIdx.x;
+  grid_dependency_wait();
+  shard_fold_decide<DL>(a, b, sm, static_cast<const char*>(all_records), record_bytes, n_shards,
+                        true);
+  if (threadIdx.x == 0 && a.mode == SPECDEC_SAMPLE) {
     a.sel[b] = sm.sr;
     a.counters[b] = 0;
   }
+}
+
+// Few sequences: decision and slice sums in one kernel, grid (slice chunks,
+// B). Every CTA of a sequence folds the records and decides (chunk 0 writes
+// the outputs), then sums its chunk's residual and p weights; the last CTA
+// of the sequence (ticket on a counter the slice's LM-head kernel zeroed)
+// adds the chunk sums in chunk order and writes the slice's pair.
+template <typename DL>
+__global__ void __launch_bounds__(kAccThreads) shard_accept_sums_kernel(const AcceptLaunch a,
+                                                                        const SampleLaunch L,
+                                                                        const void* all_records,
+                                                                        size_t record_bytes,
+                                                                        int n_shards, float* cs_p,
+                                                                        float2* shard_sums) {
+  __shared__ AcceptSmem sm;
+  __shared__ float red[kSampleThreads / 32];
+  __shared__ int s_last;
+  const int b = blockIdx.y;
+  const int chunk = blockIdx.x;
+  grid_dependency_wait();
+  shard_fold_decide<DL>(a, b, sm, static_cast<const char*>(all_records), record_bytes, n_shards,
+                        chunk == 0);
+  const SelectedRow sr = sm.sr;
+  if (chunk == 0 && threadIdx.x == 0) a.sel[b] = sr;
+  if (sr.j < 0) return;
+  const int g1 = L.gamma + 1;
+  const bool residual = sr.residual != 0;
+  const float* zr = L.z + (size_t)(b * g1 + sr.j) * L.V;
+  const DL* qr = residual ? static_cast<const DL*>(L.dl) + ((size_t)b * L.gamma + sr.j) * L.V
+                          : nullptr;
+  const bool vec = L.vec != 0;
+  const float tp = chunk_total<DL>(zr, nullptr, sr, false, L.c, L.V, vec, chunk, red);
+  const float tr = residual ? chunk_total<DL>(zr, qr, sr, true, L.c, L.V, vec, chunk, red) : tp;
+  if (threadIdx.x == 0) {
+    L.chunk_sums[(size_t)b * L.nchunks + chunk] = tr;
+    cs_p[(size_t)b * L.nchunks + chunk] = tp;
+    __threadfence();
+    s_last = atomicAdd(&L.counters[b], 1) % L.nchunks == L.nchunks - 1;
+  }
+  __syncthreads();
+  if (!s_last || threadIdx.x != 0) return;
+  __threadfence();
+  float sres = 0.f, sp = 0.f;
+  for (int k = 0; k < L.nchunks; ++k) {
+    sres += __ldcg(L.chunk_sums + (size_t)b * L.nchunks + k);
+    sp += __ldcg(cs_p + (size_t)b * L.nchunks + k);
+  }
+  shard_sums[b] = make_float2(sres, sp);
 }
 
 // Grid (slice chunks, B): the residual weights max(0, p - q) and the p
@@ -340,6 +397,22 @@ cudaError_t launch_shard_accept(const AcceptLaunch& A, const void* all_records,
   const cudaLaunchConfig_t cfg = pdl_config(dim3(A.B), kAccThreads, stream, attr);
   return cudaLaunchKernelEx(&cfg, shard_accept_kernel<__nv_bfloat16>, A, all_records,
                             record_bytes, n_shards);
+}
+
+bool shard_fused_accept_sums(int B, int nchunks) {
+  return (long long)B * nchunks <= kFusedAcceptItems;
+}
+
+cudaError_t launch_shard_accept_sums(const AcceptLaunch& A, const SampleLaunch& L0,
+                                     const void* all_records, size_t record_bytes, int n_shards,
+                                     float* cs_p, float2* shard_sums, cudaStream_t stream) {
+  SampleLaunch L = L0;
+  L.vec = (L.V % kVec == 0 && ((uintptr_t)L.z & 15u) == 0 && ((uintptr_t)L.dl & 7u) == 0) ? 1 : 0;
+  L.prefetch = 0;
+  cudaLaunchAttribute attr[1];
+  const cudaLaunchConfig_t cfg = pdl_config(dim3(L.nchunks, L.B), kAccThreads, stream, attr);
+  return cudaLaunchKernelEx(&cfg, shard_accept_sums_kernel<__nv_bfloat16>, A, L, all_records,
+                            record_bytes, n_shards, cs_p, shard_sums);
 }
 
 cudaError_t launch_shard_sums(const SampleLaunch& L0, float* cs_p, float2* shard_sums,

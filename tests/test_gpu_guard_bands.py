@@ -255,6 +255,7 @@ def test_host_entry_point_stays_inside_its_buffers(mode, pinned):
     pytest.param(4, 4, 256, 3001, (0, 1000, 3001), id="two_slices_ragged"),
     pytest.param(64, 3, 128, 3000, (0, 1499, 3000), id="row_owner_slices_ragged"),
     pytest.param(8, 4, 4096, 128256, (0, 32064, 64128, 96192, 128256), id="llama_four_slices"),
+    pytest.param(48, 3, 64, 20000, (0, 9000, 20000), id="accept_then_sums_kernels"),
 ])
 def test_vocab_parallel_calls_stay_inside_their_buffers(B, gamma, d, V, bounds, mode):
     """specdec_shard_score / _accept / _draw: every slice's workspace,

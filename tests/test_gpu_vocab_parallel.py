@@ -82,7 +82,9 @@ def _run_sharded(inp, bounds, T, seed, mode):
     (4, 4, 256, 3001, (0, 1000, 2100, 3001)),          # three uneven slices, ragged tails
     (2, 1, 64, 128, (0, 128)),                         # one slice: the single-GPU step
     (16, 4, 128, 2049, (0, 640, 1281, 1900, 2049)),    # four slices, pairs with stream-K
+    # (up to B * chunks = 128 the accept call decides and sums in one kernel)
     (64, 3, 128, 3000, (0, 1501, 3000)),               # row-owner tiles on each slice
+    (48, 3, 64, 20000, (0, 9000, 20000)),              # B * chunks > 128: accept, then sums
 ])
 def test_sharded_step_matches_the_oracle(B, gamma, d, V, bounds, mode):
     w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, temperature=0.9, sigma=0.5)

@@ -226,6 +226,7 @@ struct TcGeometry {
   int stream_k;                  // one token tile: contiguous k-iteration ranges
   int records;                   // partial records per row (grid or vocabulary tiles)
   int rowown;                    // 1: tokens on the MMA's M side (pairs, 256-row token tiles)
+  int n_acc;                     // accumulators a tile's k-slices are dealt across (swap-AB)
 };
 TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters);
 // Co-resident clusters of the kernel for this shape on the current device

@@ -14,7 +14,7 @@
 // row gives C*128 contiguous bytes per request: fewer, longer DRAM bursts,
 // which measured ~7.1 TB/s against ~6.8 TB/s for one 128-byte slice per row.
 //
-// CTA pairs: with large token tiles (BT >= 64) each SM would have to take in
+// CTA pairs: with large token tiles (BT >= 128) each SM would have to take in
 // the whole token slice for every 128-row W slice (up to twice the W
 // bytes), and that ingress, not DRAM, limited the kernel. There K = 2 CTAs
 // form a cluster and run the 2-SM MMA (tcgen05.mma.cta_group::2, M = 256):
@@ -55,7 +55,9 @@
 //   warp 0     one thread issues TMA loads of W and hidden k-slices into a
 //              ring of shared-memory stages (full/empty mbarriers).
 //   warp 1     allocates tensor memory; one thread issues tcgen05.mma into
-//              one of two TMEM accumulators and commits to mbarriers.
+//              one of two sets of TMEM accumulators (a narrow token tile
+//              deals its k-slices across up to 16 accumulators per set, for
+//              accuracy; see issue_stage) and commits to mbarriers.
 //   warps 2-9  epilogue, two groups of four (one warp per TMEM lane quarter
 //              in each) taking alternate 32-column chunks: tcgen05.ld of the
 //              accumulator, fp32 logits out, softmax / argmax partials for p.
@@ -97,7 +99,12 @@ __host__ __device__ constexpr int misc_bytes(int BT) {
   return kBarBytes + BT * (4 * (int)sizeof(PartialP) + (int)sizeof(PartialP) + (int)sizeof(PartialQ));
 }
 constexpr int kMaxDevices = 64;
-constexpr int kClusterMinBT = 64;  // token tiles from this size share hidden slices
+constexpr int kTmemCols = 512;     // tensor-memory columns per SM
+constexpr int kMaxAcc = 16;        // accumulators per tile at most (issue_stage)
+// Token tiles from this size run on CTA pairs. Single CTAs measured 1.5-2 %
+// faster at 64-96 rows (their MMAs are short and a pair adds cluster
+// waits) and the same at 128.
+constexpr int kClusterMinBT = 128;
 // Row-owner logit staging: one 32 x 32 fp32 tile (4 KB) per epilogue warp,
 // written in the 128-byte swizzled layout the bulk tensor store reads.
 constexpr int kZStageBytes = 4096;
@@ -122,6 +129,7 @@ struct TcParams {
   const unsigned long long* calls;   // the workspace's call count, mixed into the tag
   int withhold_loads;            // self-test: issue no loads, so the first wait runs out
   int z_tma;                     // row owner: logits leave through bulk tensor stores
+  int n_acc;                     // accumulators per tile, each BT columns (see issue_stage)
   EpiParams ep;
 };
 
@@ -233,24 +241,56 @@ __device__ __forceinline__ PartialQ q_chunk_stats(const __nv_bfloat16* __restric
 // spends a few instructions per MMA: one thread issues every MMA of the CTA
 // (or pair), and on shapes with narrow token tiles each MMA's tensor work is
 // short enough that the issue rate, not the tensor core, would otherwise set
-// the pace. Only the first MMA of a piece starts the accumulator afresh.
+// the pace.
+//
+// Slice c of the stage goes to accumulator (sub0 + c) mod n_acc, each
+// acc_cols columns from the last. The tensor core adds into its fp32
+// accumulator with truncation, so the error of one accumulator grows with
+// the number of additions and with the running sum's magnitude (a bias, not
+// a random walk): dealing the slices across n_acc accumulators, which the
+// epilogue adds in fp32 at the end, divides it by about n_acc. The first
+// slice a piece gives each accumulator (fresh > c) starts it afresh.
 template <int KC, bool kPair, bool kRowOwn>
 __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t ad, uint64_t bd,
-                                            uint32_t b_slice16, uint32_t idesc,
-                                            uint32_t first_accum) {
+                                            uint32_t b_slice16, uint32_t idesc, int sub0,
+                                            int n_acc, uint32_t acc_cols, int fresh) {
+  int sub = sub0;
 #pragma unroll
   for (int c = 0; c < KC; ++c) {
+    const uint32_t d = d_tmem + (uint32_t)sub * acc_cols;
 #pragma unroll
     for (int k = 0; k < kBlockK / 16; ++k) {
       const uint64_t a = ad + (uint64_t)(c * (kStageA >> 4) + 2 * k);
       const uint64_t b = bd + (uint64_t)(c * b_slice16 + 2 * k);
-      const uint32_t accum = (c == 0 && k == 0) ? first_accum : 1u;
+      const uint32_t accum = (k == 0 && c < fresh) ? 0u : 1u;
       if constexpr (kRowOwn)   // A = token rows, B = W rows
-        tc2_mma_bf16(d_tmem, b, a, idesc, accum);
+        tc2_mma_bf16(d, b, a, idesc, accum);
       else if constexpr (kPair)
-        tc2_mma_bf16(d_tmem, a, b, idesc, accum);
+        tc2_mma_bf16(d, a, b, idesc, accum);
       else
-        tc_mma_bf16(d_tmem, a, b, idesc, accum);
+        tc_mma_bf16(d, a, b, idesc, accum);
+    }
+    if (++sub == n_acc) sub = 0;
+  }
+}
+
+// The tile's logits for 16 or 32 token columns at column `col`: the sum, in
+// order, of the n_used accumulators (stride acc_cols) the piece wrote.
+template <int N>
+__device__ __forceinline__ void tmem_ld_acc(uint32_t tbase, int col, int n_used, uint32_t acc_cols,
+                                            float (&z)[N]) {
+  static_assert(N == 16 || N == 32, "16 or 32 columns");
+  if constexpr (N == 16)
+    tmem_ld16(tbase + (uint32_t)col, z);
+  else
+    tmem_ld32(tbase + (uint32_t)col, z);
+  for (int j = 1; j < n_used; ++j) {
+#pragma unroll
+    for (int h = 0; h < N / 16; ++h) {   // 16 columns at a time: fewer live registers
+      float t[16];
+      tmem_ld16(tbase + (uint32_t)j * acc_cols + (uint32_t)(col + 16 * h), t);
+#pragma unroll
+      for (int n = 0; n < 16; ++n) z[16 * h + n] += t[n];
     }
   }
 }
@@ -433,7 +473,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.BT);
+          const uint32_t d_tmem = tmem_base + (uint32_t)(acc * p.BT * p.n_acc);
+          int sub = 0;    // accumulator of the stage's first slice
+          int srel = 0;   // slices of this piece issued so far
           for (int kc = pc.kb; kc < pc.ke; ++kc) {
             const bool got = pair ? mbar_wait_cluster<true>(full_bar(s), ph, abort_flag, p.status)
                                   : mbar_wait<true>(full_bar(s), ph, abort_flag, p.status);
@@ -444,13 +486,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t ad = desc0 + (uint64_t)((uint32_t)s * stage16);
             const uint64_t bd = ad + hoff16;
-            const uint32_t fa = kc > pc.kb ? 1u : 0u;
+            const int fresh = p.n_acc - srel;   // slices c < fresh start their accumulator
+            const uint32_t acols = (uint32_t)p.BT;
             if (p.kc == 4)
-              issue_stage<4, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, fa);
+              issue_stage<4, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, sub, p.n_acc, acols, fresh);
             else if (p.kc == 2)
-              issue_stage<2, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, fa);
+              issue_stage<2, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, sub, p.n_acc, acols, fresh);
             else
-              issue_stage<1, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, fa);
+              issue_stage<1, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, sub, p.n_acc, acols, fresh);
+            srel += p.kc;
+            sub = (sub + p.kc) % p.n_acc;
             if constexpr (kPair)
               tc2_commit_mc(empty_bar(s), 3);   // the stage is free in both CTAs
             else
@@ -747,7 +792,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       tc_fence_after();
       const int n_chunks = (min(p.BT, p.M - m_base) + 15) / 16;
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.BT);
+      const uint32_t tbase =
+          tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * p.BT * p.n_acc);
+      // accumulators this piece wrote (a short stream-K piece may not reach all)
+      const int n_used = min(p.n_acc, (pc.ke - pc.kb) * p.kc);
+      const uint32_t acols = (uint32_t)p.BT;
 
       // A tile past the vocabulary (odd tile count in a cluster) has nothing to report.
       bool finish = vt < p.n_vt;
@@ -763,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         other = p.fix + ((size_t)slot * 2 + (1 - part)) * slot_floats;
         for (int c = grp; c < n_chunks; c += 2) {
           float accv[16];
-          tmem_ld16(tbase + (uint32_t)(c * 16), accv);
+          tmem_ld_acc<16>(tbase, c * 16, n_used, acols, accv);
 #pragma unroll
           for (int n = 0; n < 16; ++n) __stcg(mine + (size_t)(c * 16 + n) * kBlockV + row, accv[n]);
         }
@@ -789,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n32 = n_chunks >> 1;
         for (int c = grp; c < n32; c += 2) {
           float z[32];
-          tmem_ld32(tbase + (uint32_t)(c * 32), z);
+          tmem_ld_acc<32>(tbase, c * 32, n_used, acols, z);
           if (other != nullptr) {
 #pragma unroll
             for (int n = 0; n < 32; ++n) z[n] += __ldcg(other + (size_t)(c * 32 + n) * kBlockV + row);
@@ -810,7 +859,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if ((n_chunks & 1) && grp == (n32 & 1)) {
           const int cc = n_chunks - 1;
           float z[16];
-          tmem_ld16(tbase + (uint32_t)(cc * 16), z);
+          tmem_ld_acc<16>(tbase, cc * 16, n_used, acols, z);
           if (other != nullptr) {
 #pragma unroll
             for (int n = 0; n < 16; ++n) z[n] += __ldcg(other + (size_t)(cc * 16 + n) * kBlockV + row);
@@ -933,8 +982,14 @@ TcGeometry tc_geometry(int M, int V, int d, int num_sms, int max_clusters) {
   int stages = budget / g.stage_bytes;
   if (stages > cap) stages = cap;
   g.stages = stages;
+  // Accumulators per tile (issue_stage): as many as two sets (the epilogue
+  // drains one while the MMAs fill the other) leave room for in the 512
+  // tensor-memory columns, up to 16; the row-owner layout fills them with one.
+  g.n_acc = 1;
+  if (!g.rowown)
+    while (g.n_acc < kMaxAcc && 2 * g.BT * (g.n_acc + 1) <= kTmemCols) ++g.n_acc;
   int cols = 32;
-  while (cols < 2 * g.BT) cols <<= 1;
+  while (cols < 2 * g.BT * g.n_acc) cols <<= 1;
   g.tmem_cols = cols;
   g.smem_bytes = 1024 + g.stages * g.stage_bytes + misc_total;
   g.n_units = ((g.n_vt + g.K - 1) / g.K) * g.n_tt;
@@ -988,6 +1043,7 @@ cudaError_t launch_lmhead_tc(const TcLaunch& L, int num_sms, cudaStream_t stream
   p.calls = L.calls;
   p.withhold_loads = L.withhold_loads;
   p.z_tma = (g.rowown && L.tmap_z != nullptr) ? 1 : 0;
+  p.n_acc = g.n_acc;
   p.ep = L.ep;
   p.ep.P = g.records;
   p.ep.run = nullptr;

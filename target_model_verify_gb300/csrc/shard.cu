@@ -12,8 +12,8 @@
 //                       and the guessed tokens' logits where this slice
 //                       holds them.
 //   exchange 1          the caller all-gathers the records (rank order).
-//   accept  (each GPU)  folds the G records of every row in rank order, so
-//                       every GPU holds the same normalisers and the same
+//   accept  (each GPU)  folds the G records of every row in one fixed order,
+//                       so every GPU holds the same normalisers and the same
 //                       acceptance decisions; writes the kept prefix and
 //                       n_accepted (greedy mode: the whole result); then
 //                       sums this slice's residual weights max(0, p - q)
@@ -136,24 +136,32 @@ __device__ __forceinline__ void shard_fold_decide(const AcceptLaunch& a, int b, 
       }
     }
   }
-  // The guessed tokens and the logits from the slice that holds each.
-  if (warp == 0 && lane < gamma) {
-    const int x = a.draft_tokens[b * gamma + lane];
+  // The guessed tokens and the logits from the slice that holds each: a
+  // warp per guess, its lanes reading the slices' flags side by side.
+  for (int i = warp; i < gamma; i += kAccThreads / 32) {
+    const int x = a.draft_tokens[b * gamma + i];
     int own = -1;
     float zx = 0.f, zqx = 0.f;
-    for (int k = 0; k < n_shards && own < 0; ++k) {
-      const ShardPtrs rp = shard_ptrs(const_cast<char*>(base) + (size_t)k * record_bytes, B, gamma);
-      const ShardXRec xr = rp.X[b * gamma + lane];
-      if (xr.owned) {
-        own = k;
-        zx = xr.zx;
-        zqx = xr.zqx;
+    for (int k0 = 0; k0 < n_shards && own < 0; k0 += 32) {
+      const int k = k0 + lane;
+      ShardXRec xr{0.f, 0.f, 0, 0};
+      if (k < n_shards)
+        xr = shard_ptrs(const_cast<char*>(base) + (size_t)k * record_bytes, B, gamma)
+                 .X[b * gamma + i];
+      const unsigned owned = __ballot_sync(0xffffffffu, xr.owned != 0);
+      if (owned) {
+        const int src = __ffs(owned) - 1;
+        own = k0 + src;
+        zx = __shfl_sync(0xffffffffu, xr.zx, src);
+        zqx = __shfl_sync(0xffffffffu, xr.zqx, src);
       }
     }
-    // A token no slice holds is out of range for the whole step.
-    sm.x[lane] = own >= 0 ? x : -1;
-    sm.zx[lane] = zx;
-    sm.zqx[lane] = zqx;
+    if (lane == 0) {
+      // A token no slice holds is out of range for the whole step.
+      sm.x[i] = own >= 0 ? x : -1;
+      sm.zx[i] = zx;
+      sm.zqx[i] = zqx;
+    }
   }
   __syncthreads();
   if (warp == 0) accept_decide<DL>(a, b, sm, outputs);

@@ -74,7 +74,8 @@ CHAIN_SHAPES = [
     pytest.param(64, 4, 4096, 128256, id="llama_b64_two_tiles"),
     pytest.param(256, 4, 4096, 128256, id="llama_b256_row_owner"),
     pytest.param(1, 4, 256, 3001, id="b1_ragged_vocab"),
-    pytest.param(16, 4, 128, 2049, id="pairs_streamk_ragged"),
+    pytest.param(30, 4, 128, 2049, id="pairs_streamk_ragged"),
+    pytest.param(16, 4, 128, 2049, id="single_ctas_80_rows_ragged"),
     pytest.param(60, 4, 128, 700, id="two_tiles_ragged"),
     pytest.param(64, 3, 128, 3000, id="row_owner_streamk_ragged"),
     pytest.param(100, 4, 64, 3000, id="row_owner_two_tiles_ragged"),
@@ -106,7 +107,7 @@ def test_verify_stays_inside_its_buffers(B, gamma, d, V, mode):
 @pytest.mark.parametrize("B,gamma,d,V", [
     pytest.param(64, 3, 128, 3000, id="row_owner_bulk_stores_ragged"),
     pytest.param(100, 4, 64, 3000, id="row_owner_two_tiles_ragged"),
-    pytest.param(16, 4, 128, 2049, id="pairs_streamk_ragged"),
+    pytest.param(30, 4, 128, 2049, id="pairs_streamk_ragged"),
     pytest.param(3, 4, 256, 1000, id="single_ctas_ragged"),
 ])
 def test_debug_outputs_stay_inside_their_buffers(B, gamma, d, V, mode):

@@ -74,8 +74,10 @@ def test_tiny_fp32_sampling(seed):
     (60, 4, 128, 700, 1.3),     # M = 300: two token tiles of 160
     (1, 32, 192, 2049, 0.5),    # gamma at its maximum, ragged tail
     (7, 3, 8, 300, 1.0),        # d = 8: one zero-padded k-slice
-    (16, 4, 200, 2049, 0.9),    # M = 80: cluster pairs with 2-D boxes (d % 64 != 0), odd tile count
-    (16, 4, 128, 1920, 1.1),    # M = 80: cluster pairs with 3-D boxes, 15 tiles (one past the end)
+    (30, 4, 200, 2049, 0.9),    # M = 150: cluster pairs with 2-D boxes (d % 64 != 0), odd tile count
+    (30, 4, 128, 1920, 1.1),    # M = 150: cluster pairs with 3-D boxes, 15 tiles (one past the end)
+    (16, 4, 128, 2049, 1.0),    # M = 80: single CTAs (pairs start at 128-row tiles), 2 slices a stage
+    (22, 4, 128, 2049, 0.9),    # M = 110: single CTAs with 112-row tiles, 1 slice a stage
     (40, 4, 64, 3000, 1.0),     # M = 200: one token tile of 208, clusters, q streamed whole
     (64, 3, 128, 2049, 0.9),    # M = 256: tokens on the MMA's M side, stream-K, V % 4 != 0
     (64, 3, 200, 1000, 1.0),    # M = 256, tokens on M with 2-D boxes and a ragged k-slice
@@ -119,6 +121,28 @@ def test_llama3_8b_head(seed, mode):
 def test_gemma_e2b_head_gamma_sweep(gamma):
     w, inp = _gen(f"gemma_e2b_head_g{gamma}", 0)
     _full_check(w, inp, 0, ov.SAMPLE)
+
+
+@pytest.mark.parametrize("name,bound", [
+    ("llama3_8b_head", 1.0e-6),       # 16 accumulators (16-row token tile)
+    ("llama3_8b_head_b4", 2.0e-6),    # 8 (32-row tile)
+    ("gemma_e2b_head_g8", 1.0e-6),    # 16, d = 1536
+])
+def test_logit_error_with_dealt_accumulators(name, bound):
+    """Narrow token tiles deal each tile's k-slices across up to 16 tensor-
+    memory accumulators that the epilogue adds in fp32 (lmhead_tc.cu,
+    issue_stage). The tensor core's fp32 additions truncate, so one
+    accumulator's error grows with the count and size of its additions: a CPU
+    model of exact 16-term blocks added with truncation gives 6.5e-6 rms at
+    d = 4096 (5.4e-6 measured with one accumulator), 3.4e-7 with 16. The rms
+    logit error against fp64 must sit well under the one-accumulator figure."""
+    w, inp = _gen(name, 2)
+    _, _, dbg = parity.run_library(inp, w.temperature, 2, ov.SAMPLE)
+    z = ov.lm_head_logits(parity.to_f64(inp["hidden"]), parity.to_f64(inp["W_lm"]))
+    dz = dbg["logits"].view(w.B, w.gamma + 1, w.V).double().cpu().numpy() - z
+    rms = float(np.sqrt(np.mean(dz ** 2)))
+    print(f"{name}: logit error rms {rms:.2e}, max {np.abs(dz).max():.2e}")
+    assert rms < bound, rms
 
 
 @pytest.mark.parametrize("B", [4, 16, 64, 256])

@@ -11,11 +11,13 @@ must equal the production tokens bit for bit.
 Every sequence of each full-size shape is compared with the fp64 oracle,
 so together the cases cover each LM-head schedule in both modes:
   * llama3_8b_head      M = 5: one 16-row token tile, stream-K, single CTAs
-  * llama3_8b_head_b16  M = 80: one token tile on CTA pairs, stream-K
+  * llama3_8b_head_b16  M = 80: one 80-row token tile, stream-K, single CTAs
+  * the same at B = 32  M = 160: one token tile on CTA pairs, stream-K
   * llama3_8b_head_b64  M = 320: two token tiles of 160 on CTA pairs
   * llama3_8b_head_b256 M = 1280: five 256-row tiles, row-owner epilogue
                         with bulk tensor stores of the logits
   * head_70b_b32_g7     M = 256: one row-owner tile with stream-K, T = 0.7
+  * gemma_e2b_head_g4/_g8  V = 262,144 (64 draw chunks), d = 1536, γ = 4, 8
   * llama3_8b_head_tree26_b8: the 26-node tree walk on 8 sequences
 
 The margin rule is applied in aggregate, as stated for the verify step:
@@ -54,11 +56,14 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 CHAIN_CASES = [
-    ("llama3_8b_head", (0, 1)),
-    ("llama3_8b_head_b16", (1, 2)),
-    ("llama3_8b_head_b64", (1, 2)),
-    ("llama3_8b_head_b256", (1, 2)),
-    ("head_70b_b32_g7", (2, 3)),
+    ("llama3_8b_head", (0, 1), {}),
+    ("llama3_8b_head_b16", (1, 2), {}),
+    ("llama3_8b_head_b16", (3,), {"B": 32}),
+    ("llama3_8b_head_b64", (1, 2), {}),
+    ("llama3_8b_head_b256", (1, 2), {}),
+    ("head_70b_b32_g7", (2, 3), {}),
+    ("gemma_e2b_head_g4", (0, 1), {}),
+    ("gemma_e2b_head_g8", (0, 1), {}),
 ]
 TREE_CASES = [("llama3_8b_head_tree26_b8", (1, 2))]
 MIN_SEQUENCES = 1000
@@ -80,9 +85,11 @@ def _near_margin(seq_result, mode) -> bool:
     return min([seq_result.sample_margin] + list(seq_result.accept_margins)) < parity.SAMPLE_MARGIN
 
 
-def _chain_case(name, seed, tally, dz_stats):
+def _chain_case(name, seed, over, tally, dz_stats):
     import target_model_verify_gb300 as tv
-    w = wl.get(name)
+    w = wl.get(name, **over)
+    if over:
+        name = name + "(" + ",".join(f"{k}={v}" for k, v in over.items()) + ")"
     inp = wl.generate(w, seed, device=DEV)
     T = w.temperature
     # The oracle's logits once per input set, shared by both modes.
@@ -149,9 +156,9 @@ def _tree_case(name, seed, tally):
 def test_production_tokens_every_sequence_full_vocabulary():
     tally = []
     dz_stats = []
-    for name, seeds in CHAIN_CASES:
+    for name, seeds, over in CHAIN_CASES:
         for seed in seeds:
-            _chain_case(name, seed, tally, dz_stats)
+            _chain_case(name, seed, over, tally, dz_stats)
     for name, seeds in TREE_CASES:
         for seed in seeds:
             _tree_case(name, seed, tally)

@@ -81,7 +81,7 @@ def _run_sharded(inp, bounds, T, seed, mode):
 @pytest.mark.parametrize("B,gamma,d,V,bounds", [
     (4, 4, 256, 3001, (0, 1000, 2100, 3001)),          # three uneven slices, ragged tails
     (2, 1, 64, 128, (0, 128)),                         # one slice: the single-GPU step
-    (16, 4, 128, 2049, (0, 640, 1281, 1900, 2049)),    # four slices, pairs with stream-K
+    (30, 4, 128, 2049, (0, 640, 1281, 1900, 2049)),    # four slices, pairs with stream-K
     # (up to B * chunks = 128 the accept call decides and sums in one kernel)
     (64, 3, 128, 3000, (0, 1501, 3000)),               # row-owner tiles on each slice
     (48, 3, 64, 20000, (0, 9000, 20000)),              # B * chunks > 128: accept, then sums

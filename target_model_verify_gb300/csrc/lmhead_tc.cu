@@ -250,14 +250,18 @@ __device__ __forceinline__ PartialQ q_chunk_stats(const __nv_bfloat16* __restric
 // a random walk): dealing the slices across n_acc accumulators, which the
 // epilogue adds in fp32 at the end, divides it by about n_acc. The first
 // slice a piece gives each accumulator (fresh > c) starts it afresh.
-template <int KC, bool kPair, bool kRowOwn>
+//
+// kMulti = false (one accumulator) compiles to the plain loop: the issuing
+// thread's own instructions are on the critical path of the tensor-bound
+// shapes, so nothing here may cost more than a few per MMA.
+template <int KC, bool kPair, bool kRowOwn, bool kMulti>
 __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t ad, uint64_t bd,
                                             uint32_t b_slice16, uint32_t idesc, int sub0,
                                             int n_acc, uint32_t acc_cols, int fresh) {
   int sub = sub0;
 #pragma unroll
   for (int c = 0; c < KC; ++c) {
-    const uint32_t d = d_tmem + (uint32_t)sub * acc_cols;
+    const uint32_t d = kMulti ? d_tmem + (uint32_t)sub * acc_cols : d_tmem;
 #pragma unroll
     for (int k = 0; k < kBlockK / 16; ++k) {
       const uint64_t a = ad + (uint64_t)(c * (kStageA >> 4) + 2 * k);
@@ -270,7 +274,7 @@ __device__ __forceinline__ void issue_stage(uint32_t d_tmem, uint64_t ad, uint64
       else
         tc_mma_bf16(d, a, b, idesc, accum);
     }
-    if (++sub == n_acc) sub = 0;
+    if (kMulti && ++sub == n_acc) sub = 0;
   }
 }
 
@@ -457,6 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t stage16 = p.stage_bytes >> 4;
         const uint32_t hoff16 = (uint32_t)(p.kc * kStageA) >> 4;
         const uint32_t hsl16 = (uint32_t)(hid_rows * kBlockK * 2) >> 4;
+        const int n_acc = p.n_acc, kcs = p.kc;
+        const uint32_t acols = (uint32_t)p.BT;
         int s = 0;
         uint32_t ph = 0;
         int ul = 0;
@@ -486,16 +492,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const uint64_t ad = desc0 + (uint64_t)((uint32_t)s * stage16);
             const uint64_t bd = ad + hoff16;
-            const int fresh = p.n_acc - srel;   // slices c < fresh start their accumulator
-            const uint32_t acols = (uint32_t)p.BT;
-            if (p.kc == 4)
-              issue_stage<4, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, sub, p.n_acc, acols, fresh);
-            else if (p.kc == 2)
-              issue_stage<2, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, sub, p.n_acc, acols, fresh);
-            else
-              issue_stage<1, kPair, kRowOwn>(d_tmem, ad, bd, hsl16, idesc, sub, p.n_acc, acols, fresh);
-            srel += p.kc;
-            sub = (sub + p.kc) % p.n_acc;
+            const int fresh = n_acc - srel;   // slices c < fresh start their accumulator
+            if (n_acc == 1) {
+              if (kcs == 4)
+                issue_stage<4, kPair, kRowOwn, false>(d_tmem, ad, bd, hsl16, idesc, 0, 1, acols, fresh);
+              else if (kcs == 2)
+                issue_stage<2, kPair, kRowOwn, false>(d_tmem, ad, bd, hsl16, idesc, 0, 1, acols, fresh);
+              else
+                issue_stage<1, kPair, kRowOwn, false>(d_tmem, ad, bd, hsl16, idesc, 0, 1, acols, fresh);
+            } else {
+              if (kcs == 4)
+                issue_stage<4, kPair, kRowOwn, true>(d_tmem, ad, bd, hsl16, idesc, sub, n_acc, acols, fresh);
+              else if (kcs == 2)
+                issue_stage<2, kPair, kRowOwn, true>(d_tmem, ad, bd, hsl16, idesc, sub, n_acc, acols, fresh);
+              else
+                issue_stage<1, kPair, kRowOwn, true>(d_tmem, ad, bd, hsl16, idesc, sub, n_acc, acols, fresh);
+              sub += kcs;   // kcs <= 4, so a few subtractions replace a division
+              while (sub >= n_acc) sub -= n_acc;
+            }
+            srel += kcs;
             if constexpr (kPair)
               tc2_commit_mc(empty_bar(s), 3);   // the stage is free in both CTAs
             else

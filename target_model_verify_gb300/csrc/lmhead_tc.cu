@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(tfull_bar(a), 1);
-      mbar_init(tempty_bar(a), pair ? 2 * kEpiThreads : kEpiThreads);   // a pair's leader counts both epilogues
+      mbar_init(tempty_bar(a), pair ? 2 : 1);   // one arrival per epilogue; a pair's leader counts both
     }
     mbar_init(mma_done_bar, 1);
     *abort_flag = 0;
@@ -747,11 +747,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
+      // Every epilogue thread's tensor-memory loads are done; one thread per
+      // CTA hands the accumulator back.
       tc_fence_before();
-      if (rank == 1)
-        mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
-      else
-        mbar_arrive(tempty_bar(acc));
+      named_bar_sync(1, kEpiThreads);
+      if (threadIdx.x == 64) {
+        if (rank == 1)
+          mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+        else
+          mbar_arrive(tempty_bar(acc));
+      }
       if (!p.stream_k) {
         // One record per (token row, vocabulary tile): merge the two groups.
         if (grp == 1) red[r] = st;
@@ -908,11 +913,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         named_bar_sync(1, kEpiThreads);
       }
+      // Every epilogue thread's tensor-memory loads are done; one thread per
+      // CTA hands the accumulator back (a pair's to the leader, whose MMAs
+      // reuse it).
       tc_fence_before();
-      if (pair && rank == 1)
-        mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));   // the leader's MMA reuses it
-      else
-        mbar_arrive(tempty_bar(acc));
+      named_bar_sync(1, kEpiThreads);
+      if (epi_tid == 0) {
+        if (pair && rank == 1)
+          mbar_arrive_remote(mapa_shared(tempty_bar(acc), 0));
+        else
+          mbar_arrive(tempty_bar(acc));
+      }
     }
     if (p.stream_k) {
       // One record per token row for everything this CTA finished.

@@ -85,6 +85,7 @@ def _run_sharded(inp, bounds, T, seed, mode):
     # (up to B * chunks = 128 the accept call decides and sums in one kernel)
     (64, 3, 128, 3000, (0, 1501, 3000)),               # row-owner tiles on each slice
     (48, 3, 64, 20000, (0, 9000, 20000)),              # B * chunks > 128: accept, then sums
+    (4, 3, 64, 3000, tuple(3000 * g // 40 for g in range(41))),   # 40 slices: two lanes' worth
 ])
 def test_sharded_step_matches_the_oracle(B, gamma, d, V, bounds, mode):
     w = wl.get("llama3_8b_head", B=B, gamma=gamma, d=d, V=V, temperature=0.9, sigma=0.5)

@@ -106,3 +106,32 @@ def test_tree_workspace_and_host_side_errors(lib):
     assert _tree_call(ws_bytes=16) == b.SPECDEC_ERR_WORKSPACE
     assert _tree_call(B=0) == b.SPECDEC_OK
     assert _tree_call(mode=1, dl=0, T=0.0, ws=0) == b.SPECDEC_ERR_WORKSPACE    # greedy: no q, no T
+
+
+def test_shard_sizes_and_host_side_argument_errors(lib):
+    """The vocabulary-parallel calls check their arguments on the host."""
+    assert b.specdec_shard_record_bytes(256, 4) >= 256 * 5 * 16 + 256 * 4 * (8 + 16)
+    assert b.specdec_shard_record_bytes(1, 0) == 0
+    assert b.specdec_shard_workspace_size(1, 4, 4096, 32064, 0) > 5 * 32064 * 4
+    assert b.specdec_shard_workspace_size(1, 4, 4090, 32064, 0) == 0     # d % 8 != 0
+    ws, ptr = 4096 * 256, 4096
+    big = 1 << 30
+    # score: the slice must sit inside [0, V); temperature must be positive
+    assert b.specdec_shard_score(ptr, ptr, ptr, ptr, 1, 4, 64, 500, 600, 1000, 1.0, 0, ptr, ws, big,
+                                 None) == b.SPECDEC_ERR_UNSUPPORTED
+    assert b.specdec_shard_score(ptr, ptr, ptr, ptr, 1, 4, 64, 500, 0, 1000, 0.0, 0, ptr, ws, big,
+                                 None) == b.SPECDEC_ERR_INVALID_ARG
+    assert b.specdec_shard_score(ptr, ptr, ptr, ptr, 1, 4, 64, 500, 0, 1000, 1.0, 0, ptr, 300, big,
+                                 None) == b.SPECDEC_ERR_WORKSPACE
+    # accept: 1 <= n_shards <= SPECDEC_MAX_SHARDS
+    for n in (0, 65):
+        assert b.specdec_shard_accept(ptr, n, ptr, ptr, 1, 4, 64, 500, 0, 1000, 1.0, 0, 0, ptr, ptr,
+                                      ptr, ws, big, None) == b.SPECDEC_ERR_INVALID_ARG
+    # draw: the caller's slice index must be one of the n_shards
+    assert b.specdec_shard_draw(ptr, 2, 2, ptr, 1, 4, 64, 500, 0, 1000, 1.0, 0, 0, ptr, ws, big,
+                                None) == b.SPECDEC_ERR_INVALID_ARG
+    assert b.specdec_shard_draw(ptr, 2, -1, ptr, 1, 4, 64, 500, 0, 1000, 1.0, 0, 0, ptr, ws, big,
+                                None) == b.SPECDEC_ERR_INVALID_ARG
+    # greedy mode has nothing to draw: the call is a no-op
+    assert b.specdec_shard_draw(0, 0, 0, 0, 1, 4, 64, 500, 0, 1000, 1.0, 0, 1, 0, ws, big,
+                                None) == b.SPECDEC_OK

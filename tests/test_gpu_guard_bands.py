@@ -77,6 +77,8 @@ CHAIN_SHAPES = [
     pytest.param(30, 4, 128, 2049, id="pairs_streamk_ragged"),
     pytest.param(16, 4, 128, 2049, id="single_ctas_80_rows_ragged"),
     pytest.param(60, 4, 128, 700, id="two_tiles_ragged"),
+    pytest.param(40, 4, 64, 3000, id="pairs_208_rows_ragged"),
+    pytest.param(22, 4, 128, 2049, id="single_ctas_112_rows_ragged"),
     pytest.param(64, 3, 128, 3000, id="row_owner_streamk_ragged"),
     pytest.param(100, 4, 64, 3000, id="row_owner_two_tiles_ragged"),
 ]
@@ -109,6 +111,8 @@ def test_verify_stays_inside_its_buffers(B, gamma, d, V, mode):
     pytest.param(100, 4, 64, 3000, id="row_owner_two_tiles_ragged"),
     pytest.param(30, 4, 128, 2049, id="pairs_streamk_ragged"),
     pytest.param(3, 4, 256, 1000, id="single_ctas_ragged"),
+    pytest.param(40, 4, 64, 3000, id="pairs_208_rows_ragged"),
+    pytest.param(22, 4, 128, 3000, id="single_ctas_112_rows_ragged"),
 ])
 def test_debug_outputs_stay_inside_their_buffers(B, gamma, d, V, mode):
     """The debug call writes the logits into the caller's buffer (through the

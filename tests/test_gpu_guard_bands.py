@@ -151,6 +151,7 @@ def test_debug_outputs_stay_inside_their_buffers(B, gamma, d, V, mode):
 @pytest.mark.parametrize("name,over", [
     pytest.param("llama3_8b_head_tree26_b8", {}, id="tree26_b8_full"),
     pytest.param("llama3_8b_head_tree26", {"d": 128, "V": 3001}, id="tree26_ragged"),
+    pytest.param("llama3_8b_head_tree26_b8", {"d": 128, "V": 3000}, id="tree26_b8_vector_loads"),
 ])
 def test_tree_stays_inside_its_buffers(name, over, mode):
     import target_model_verify_gb300 as tv

@@ -45,7 +45,7 @@ LMHEAD_SOURCES = ["target_model_verify_gb300/csrc/lmhead_tc.cu",
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ncu_traffic.json")
 CPU_BASELINE_SECONDS = 10.0
 CLOCK_WINDOW_SECONDS = 1.5
-REFERENCE_BUDGET_SECONDS = 150.0
+REFERENCE_SECONDS_PER_RUN = 150.0
 
 
 def parse_args(argv=None):
@@ -209,7 +209,7 @@ def blas_threads():
     return int(get()) if get is not None else None
 
 
-def time_oracle_one_thread(w, inp, mode, budget_s: float):
+def time_oracle_one_thread(w, inp, mode, seconds: float):
     """time_oracle with NumPy's BLAS limited to one thread (restored after)."""
     get, set_ = _openblas_fns()
     if get is None:
@@ -217,7 +217,7 @@ def time_oracle_one_thread(w, inp, mode, budget_s: float):
     n0 = int(get())
     set_(1)
     try:
-        return time_oracle(w, inp, mode, budget_s)
+        return time_oracle(w, inp, mode, seconds)
     finally:
         set_(n0)
 
@@ -255,12 +255,12 @@ def oracle_step(w, h, W, x, dl, seed, mode):
     return ov.verify(h, W, x, dl, w.temperature, seed, mode)
 
 
-def time_oracle(w, inp, mode, budget_s: float, min_steps: int = 1):
-    """Full oracle steps on the host cores until the budget is used."""
+def time_oracle(w, inp, mode, seconds: float, min_steps: int = 1):
+    """Full oracle steps on the host cores until `seconds` have passed."""
     h, W, x, dl = oracle_inputs(inp, mode)
     n = 0
     t0 = time.perf_counter()
-    while n < min_steps or time.perf_counter() - t0 < budget_s:
+    while n < min_steps or time.perf_counter() - t0 < seconds:
         oracle_step(w, h, W, x, dl, 1000 + n, mode)
         n += 1
     return n / (time.perf_counter() - t0), n
@@ -569,12 +569,12 @@ def run_reference(args, world, rank, local):
     device = "cuda" if torch.cuda.is_available() else "cpu"
     inp = (wl.generate_tree if w.tree is not None else wl.generate)(w, args.seed, device=device)
     h, W, x, dl = oracle_inputs(inp, mode)
-    # One full step, to size the per-step sample so the run fits the budget.
+    # One full step, to size the per-step sample so the run fits its time allowance.
     t0 = time.perf_counter()
     oracle_step(w, h, W, x, dl, 0, mode)
     t_full = time.perf_counter() - t0
     n_total = args.steps + args.warmup
-    frac = min(1.0, REFERENCE_BUDGET_SECONDS / max(n_total * t_full, 1e-9))
+    frac = min(1.0, REFERENCE_SECONDS_PER_RUN / max(n_total * t_full, 1e-9))
     Vs = max(1, int(w.V * frac))
     Ws = W[:Vs]
     xs = np.minimum(x, Vs - 1)

@@ -133,3 +133,52 @@ def test_sharded_token_out_of_range_sets_status():
     assert tv.read_status(shards[0].workspace) == tv._b.SPECDEC_ERR_TOKEN_RANGE
     assert int(nacc[1]) == -1 and bool((out[1] == -1).all())
     assert int(nacc[0]) >= 0 and int(nacc[2]) >= 0
+
+
+def test_sharded_committed_token_law():
+    """Distribution preservation through the vocabulary-parallel step: with
+    the vocabulary split in four uneven slices, 2 * 10^5 draws (10^4
+    identical rows x 20 calls, each its own seed) of the first written token
+    follow p0 (chi-square), and the kept fraction is sum min(p0, q0) ("推测解码",
+    sections 和大模型写的一样 and 接受率 α). The acceptance test and the draw
+    both cross slices: the guesses land in every slice, and the replacement
+    is drawn from the slices' running sums."""
+    import math
+    stats = pytest.importorskip("scipy.stats")
+    import target_model_verify_gb300 as tv
+    V, d, B, calls = 64, 64, 10000, 20
+    bounds = (0, 9, 30, 47, 64)
+    w = wl.get("llama3_8b_head", B=1, gamma=1, d=d, V=V, sigma=0.8, w_std=0.3)
+    base = wl.generate(w, 123, device=DEV)
+    hidden = base["hidden"].expand(B, -1, -1).contiguous()
+    dl = base["draft_logits"].expand(B, -1, -1).contiguous()
+    res1 = parity.run_oracle(base, 1.0, 0, ov.SAMPLE)
+    p0, _ = ov.softmax_t(res1.z[0, 0], 1.0)
+    q0, _ = ov.softmax_t(parity.to_f64(base["draft_logits"])[0, 0], 1.0)
+    rng = np.random.default_rng(6)
+    G = len(bounds) - 1
+    shards = [tv.VocabShard(base["W_lm"][a:b].contiguous(), a, V, B, 1, ov.SAMPLE, 1.0)
+              for a, b in zip(bounds[:-1], bounds[1:])]
+    dls = [dl[:, :, a:b].contiguous() for a, b in zip(bounds[:-1], bounds[1:])]
+    counts = np.zeros(V)
+    kept = 0
+    for c in range(calls):
+        x = torch.as_tensor(rng.choice(V, size=(B, 1), p=q0), dtype=torch.int32, device=DEV)
+        recs = torch.cat([sh.score(hidden, x, dls[g]).clone() for g, sh in enumerate(shards)])
+        outs, sums, nacc = [], [], None
+        for g, sh in enumerate(shards):
+            o = torch.empty(B, 2, dtype=torch.int32, device=DEV)
+            n = torch.empty(B, dtype=torch.int32, device=DEV)
+            sums.append(sh.accept(recs, G, x, dls[g], 1000 + c, o, n).clone().reshape(-1))
+            outs.append(o)
+            nacc = n
+        all_sums = torch.cat(sums)
+        for g, sh in enumerate(shards):
+            sh.draw(all_sums, G, g, dls[g], 1000 + c, outs[g])
+        out = torch.stack(outs).amax(dim=0)
+        counts += np.bincount(out[:, 0].cpu().numpy(), minlength=V)
+        kept += int((nacc == 1).sum())
+    n = B * calls
+    assert stats.chisquare(counts, p0 * n).pvalue > 1e-4
+    alpha = np.minimum(p0, q0).sum()
+    assert abs(kept / n - alpha) < 4 * math.sqrt(alpha * (1 - alpha) / n)

@@ -815,7 +815,7 @@ def run_cluster_head(args):
         "roofline": {"bound": "hbm", "achieved": bytes_read / (us * 1e-6) / 1e9,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": bytes_read / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
-                     "algorithmic_bytes": bytes_read, "kernel": "cluster head (4 kernels)",
+                     "algorithmic_bytes": bytes_read, "kernel": "cluster head (3 kernels with one kept cluster and up to 8 rows, else 4)",
                      "peak_source": f"{kind} (MEASURED_PEAKS.json)"},
         "cpu_baseline": cpu,
         "config": {"M": M, "top_k": K, "V": V, "d": d, "clusters": n_c, "cluster_size": size,

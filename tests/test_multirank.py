@@ -75,3 +75,19 @@ def test_reference_arm_under_torchrun_prints_once_from_rank_zero():
     assert rec["impl"] == "reference"
     assert rec["n_gpus"] == 2
     assert rec["unit"] == "steps/s" and rec["value"] > 0
+    # The keys of the benchmark line that the reference arm shares with the
+    # library's arm, with the values this arm must carry.
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in rec, key
+    assert (rec["steps"], rec["warmup"]) == (3, 3)
+    assert rec["higher_is_better"] is True and rec["scaling"] == "weak"
+    assert rec["vs_baseline"] is None and rec["dtype"] == "f64"
+    assert rec["ms_per_step"] == pytest.approx(1e3 / rec["value"], rel=1e-6)
+    assert rec["config"]["workload"] == "tiny_fp32"
+    cpu = rec["cpu_baseline"]
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == rec["value"]
+    assert isinstance(cpu["sample"], str) and cpu["sample"]
+    assert rec["e2e"] == {"value": rec["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
+                          "d2h_bytes_per_step": 0}

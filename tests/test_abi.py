@@ -135,3 +135,31 @@ def test_shard_sizes_and_host_side_argument_errors(lib):
     # greedy mode has nothing to draw: the call is a no-op
     assert b.specdec_shard_draw(0, 0, 0, 0, 1, 4, 64, 500, 0, 1000, 1.0, 0, 1, 0, ws, big,
                                 None) == b.SPECDEC_OK
+
+
+def test_bench_launch_count_follows_the_library_plan():
+    """bench.py reports gpu_launches from its own copy of the launch plan
+    (two kernels while B * chunks fits the fused acceptance-and-draw kernel,
+    three up to the one-kernel sampler's limit, else four). Its thresholds
+    must be the library's, read here from the kernel sources."""
+    import os
+    import re
+    import bench
+    from target_model_verify_gb300 import workloads as wl
+    csrc = os.path.join(os.path.dirname(libbuild.__file__), "csrc")
+    text = "".join(open(os.path.join(csrc, f)).read() for f in ("common.cuh", "kernels.h"))
+
+    def constant(name):
+        m = re.search(r"constexpr\s+(?:long\s+long|int)\s+%s\s*=\s*(\d+)\s*;" % name, text)
+        assert m, name
+        return int(m.group(1))
+
+    assert bench.SAMPLE_CHUNK == constant("kChunkV")
+    assert bench.FUSED_ITEMS == constant("kFusedAcceptItems")
+    assert bench.ONE_DRAW_KERNEL_ITEMS == constant("kSampleOneKernelItems")
+    expect = {"llama3_8b_head": 2, "llama3_8b_head_b4": 2, "llama3_8b_head_b16": 3,
+              "llama3_8b_head_b64": 4, "llama3_8b_head_b256": 4, "head_70b_b32_g7": 4,
+              "gemma_e2b_head_g1": 2}
+    for name, n in expect.items():
+        assert bench.kernels_per_step(wl.get(name), wl.SAMPLE) == n, name
+        assert bench.kernels_per_step(wl.get(name), wl.GREEDY) == 2, name

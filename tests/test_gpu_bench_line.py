@@ -66,7 +66,10 @@ def test_bench_line_arithmetic(line):
     # A copy-bandwidth peak can be beaten a little, not by much; far below
     # it the kernel would not be streaming W.
     assert 0.5 < roof["frac"] < 1.15, roof
-    assert roof["kernel_us"] < 1e3 * r["ms_per_step"]   # the LM head is part of the step
+    # The LM head is part of the step. Its events sit between kernels, so its
+    # time also holds the launch latency that back-to-back steps overlap
+    # with the previous step's tail: a few percent of slack.
+    assert roof["kernel_us"] < 1.03e3 * r["ms_per_step"]
     if roof["traffic"] is not None:
         assert roof["traffic"] >= 0.99 * lm_bytes
     assert 0.0 < r["step_roofline"]["frac"] <= 1.05

@@ -36,10 +36,10 @@ cases, greedy and sampling apart:
     fp64 oracle's by ~5e-6 rms (printed below); propagated through p (and
     through max(0, p - q), normalised by a residual mass of ~0.35) that
     moves the boundaries by ~3e-9 to ~1e-8 each, i.e. ~0.5-1 % of sampled
-    sequences, every one of them at an oracle margin below 1e-4. (Drawing
-    with fp64-accurate sums instead of the library's fp32 hierarchical sums
-    measured 7 instead of 9 excused of 754: within the noise of this floor.)
-    The bound sits above that band.
+    sequences, every one of them at an oracle margin below 1e-4. The
+    sampler's fp32 prefix sums add a comparable share: exact integer prefix
+    sums measured 6 instead of 9 excused of 790. The bound sits above that
+    band.
 """
 import numpy as np
 import pytest
